@@ -1,0 +1,21 @@
+"""CPU oracle for sequence-parallel exact attention (TEST INFRASTRUCTURE ONLY).
+
+This package is a plain, slow, fp64 NumPy statement of what the GPU library
+computes. It exists so tests can check the CUDA path against something whose
+correctness can be read off the page by eye. Only `tests/`, the package's
+smoke check and the benchmark's CPU-baseline leg may import it; the library
+itself never does, and it shares no code with the CUDA path.
+
+Modules
+  attention  exact masked softmax attention and its gradient (the definition)
+  layouts    contiguous / zigzag / stripe sequence permutations and the
+             Ulysses sequence<->head all-to-all, as index maps
+  merge      the associative log-sum-exp merge of (O, LSE) partials
+  ring       a ring simulator: per-chunk partials in ring order + merge
+
+Every function is pinned by `-m "not gpu"` tests against something other than
+itself (brute force, a library routine, finite differences, closed forms and
+the worked examples printed on the pages). No function here is "parity
+unpinned".
+"""
+from . import attention, layouts, merge, ring  # noqa: F401
