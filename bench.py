@@ -1,0 +1,439 @@
+"""Benchmark of the sequence-parallel attention hot path on GB300.
+
+One step is one training pass of the whole path over one batch of synthetic
+input, through the library's C ABI:
+  extract q, k, v, dO into rank-major order (layout permute)
+  -> usp_attn_fwd  (Ulysses seq->head exchange, ring attention with the
+                    fused LSE merge, head->seq exchange)
+  -> usp_attn_bwd  (exchanges, Delta, dQ/dK/dV with the ring return)
+  -> restore O, dQ, dK, dV to natural order.
+The metric is useful attention TFLOP/s (masked pairs not counted; backward
+= 2.5x forward). The standalone tree/linear LSE merge is timed on its own
+workload in the same run and reported under "merge".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torchrun; every rank runs its own replica of the
+workload (the virtual ranks already live in one GPU), scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("causal attn TFLOP/s (useful FLOPs) & % of GB300 BF16 dense peak, "
+          "S=8K–128K")
+DEFAULT_WORKLOAD = "usp_ud2_ring4_s8k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+KERNEL_SOURCES = {
+    "attn_fwd_tc": "attn_fwd_tc.cu", "attn_bwd_tc": "attn_bwd_tc.cu",
+    "attn_fwd_simt": "attn_simt.cu", "attn_bwd_dq_simt": "attn_simt.cu",
+    "attn_bwd_dkdv_simt": "attn_simt.cu", "attn_bwd_preprocess": "attn_simt.cu",
+    "permute_layout": "permute.cu", "permute_ulysses": "permute.cu",
+    "merge_linear": "merge.cu", "merge_tree": "merge.cu",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(kernel: str):
+    src = KERNEL_SOURCES.get(kernel)
+    if not src:
+        return None
+    path = os.path.join(ROOT, "sequence_long_context_gb300", "csrc", src)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the capture; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = source_hash(kernel)
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and parts[0] == kernel and parts[1] == workload \
+                    and parts[2] == want:
+                return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = f"/tmp/usp_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_sample(w, seed: int, budget_s: float):
+    """Time the CPU oracle (as it stands) on a bounded sample of workload w:
+    forward + backward of one (batch 0, head 0) pair, on the longest causal
+    prefix of the sequence that fits the time budget. Returns
+    (useful TFLOP/s, seconds, sample description, threads)."""
+    import numpy as np
+    import torch
+
+    from oracle import attention
+    from sequence_long_context_gb300 import flops
+    from sequence_long_context_gb300.workloads import make_inputs
+
+    one = w.replace(B=1, Hq=1, Hkv=1, ud=1, varlen=False)
+    x = make_inputs(one.replace(S=w.S), seed=seed, with_grad=w.backward)
+    S = w.S
+    while True:
+        # estimate from a quarter-length run, scale by the pair count ratio
+        t0 = time.perf_counter()
+        s_small = max(64, S // 4)
+        sl = {k: v[:, :s_small] for k, v in x.items() if k != "cu_seqlens"}
+        attention.attn_fwd(sl["q"], sl["k"], sl["v"], w.scale, w.causal, w.window, w.sink_tokens)
+        t_small = time.perf_counter() - t0
+        est = t_small * (S / s_small) ** 2 * (3.5 if w.backward else 1.0)
+        if est <= budget_s or S <= 256:
+            break
+        S //= 2
+    sl = {k: v[:, :S] for k, v in x.items() if k != "cu_seqlens"}
+    t0 = time.perf_counter()
+    attention.attn_fwd(sl["q"], sl["k"], sl["v"], w.scale, w.causal, w.window, w.sink_tokens)
+    if w.backward:
+        attention.attn_bwd(sl["q"], sl["k"], sl["v"], sl["dout"], w.scale, w.causal,
+                           w.window, w.sink_tokens)
+    dt = time.perf_counter() - t0
+    f = flops.attention_flops(one.replace(S=S))["total"]
+    threads = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_info
+        blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        threads = min(threads, blas) if blas else threads
+    except Exception:
+        pass
+    desc = (f"fp64 NumPy oracle, batch 0 head 0 of {w.name}, causal prefix "
+            f"S={S} of {w.S}, {'fwd+bwd' if w.backward else 'fwd'} "
+            f"(1 of {w.B * w.Hq if not w.varlen else w.Hq} (batch, head) pairs)")
+    return f / dt / 1e12, dt, desc, threads
+
+
+def run_reference(args):
+    """The oracle timed on the host cores, as the reference arm."""
+    import numpy as np  # noqa: F401
+
+    from sequence_long_context_gb300.workloads import WORKLOADS
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    vals, times = [], []
+    desc, thr = "", 0
+    for i in range(args.warmup + args.steps):
+        v, dt, desc, thr = oracle_sample(w, args.seed, budget)
+        if i >= args.warmup:
+            vals.append(v)
+            times.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import sequence_long_context_gb300 as usp
+    from sequence_long_context_gb300 import flops
+    from sequence_long_context_gb300.workloads import WORKLOADS, make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build() if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+        __graft_entry__.build()
+
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w, seed=args.seed + rank, device=str(dev))
+    cu = x.get("cu_seqlens")
+    cu_dev = cu.to(dev) if cu is not None else None
+    F = flops.attention_flops(w, cu.tolist() if cu is not None else None)
+    names = ["q", "k", "v"] + (["dout"] if w.backward else [])
+    kw = dict(causal=w.causal, window=w.window, sink_tokens=w.sink_tokens,
+              cu_seqlens=cu_dev, cp=w.cp, ud=w.ud, layout=w.layout)
+
+    def step(inp):
+        qp, kp, vp = (usp.permute(inp[n], "extract", w.layout, w.cp) for n in "qkv")
+        out, lse = usp.attn_forward(qp, kp, vp, **kw)
+        res = [out]
+        if w.backward:
+            dop = usp.permute(inp["dout"], "extract", w.layout, w.cp)
+            res += list(usp.attn_backward(qp, kp, vp, out, lse, dop, **kw))
+        return [usp.permute(r, "restore", w.layout, w.cp) for r in res]
+
+    def timed(fn, n):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(n):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms = a.elapsed_time(b) / n
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    for _ in range(args.warmup):
+        step(x)
+    torch.cuda.synchronize()
+
+    # device-resident timed region (inputs 4 x 128 MiB > L2: no flush needed)
+    usp.usp_profile_enable(True)
+    l0 = usp.usp_launch_count()
+    with ClockSampler(local) as clk:
+        ms = timed(lambda: step(x), args.steps)
+    launches = (usp.usp_launch_count() - l0) // args.steps
+    usp.usp_profile_enable(False)
+    kstats = usp.usp_profile_read()
+    clocks = clk.summary()
+
+    pk, pk_src = peaks()
+    timed_s = ms * args.steps / 1e3
+    tensor_peak = pk["bf16_tflops_sustained"] if timed_s > 2.0 else pk["bf16_tflops"]
+    tensor_peak_name = "bf16_tflops_sustained" if timed_s > 2.0 else "bf16_tflops"
+    kernels = {}
+    for name, (n, tot) in sorted(kstats.items()):
+        avg = tot / max(n, 1)
+        kernels[name] = {"launches_per_step": n / args.steps, "avg_ms": avg,
+                         "share": tot / max(1e-9, sum(t for _, t in kstats.values()))}
+    # dominant kernel and its algorithmic work per launch
+    fwd_k = [k for k in kernels if k.startswith("attn_fwd")]
+    bwd_k = [k for k in kernels if k.startswith("attn_bwd") and "preprocess" not in k]
+    cand = []
+    for k in fwd_k:
+        cand.append((kstats[k][1], k, F["fwd"]))
+    if bwd_k:
+        tot_bwd = sum(kstats[k][1] for k in bwd_k)
+        nb = kstats[bwd_k[0]][0]
+        cand.append((tot_bwd, "+".join(bwd_k), F["bwd"]))
+    dom = max(cand) if cand else None
+    roofline = None
+    if dom:
+        tot_ms, name, work = dom
+        n_launch = kstats[name.split("+")[0]][0]
+        avg_ms = tot_ms / max(n_launch, 1)
+        achieved = work / (avg_ms * 1e-3) / 1e12
+        roofline = {"kernel": name, "bound": "tensor", "achieved": achieved,
+                    "peak": tensor_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tensor_peak,
+                    "traffic": traffic_for(name.split("+")[0], w.name),
+                    "peak_source": f"{pk_src} {tensor_peak_name}",
+                    "work_per_launch": work, "avg_ms": avg_ms}
+    # HBM kernels: algorithmic bytes per launch
+    elem = 2 if w.dtype == "bf16" else 4
+    q_bytes = (1 if w.varlen else w.B) * w.S * w.Hq * w.D * elem
+    kv_bytes = (1 if w.varlen else w.B) * w.S * w.Hkv * w.D * elem
+    # tensor bytes moved per step by each permute family (each byte is read
+    # once and written once): extract q,k,v(,dO), restore O(,dQ,dK,dV); the
+    # Ulysses exchange inside the attention calls when ud > 1.
+    if w.backward:
+        moved = {"permute_layout": 4 * q_bytes + 4 * kv_bytes,
+                 "permute_ulysses": 6 * q_bytes + 6 * kv_bytes}
+    else:
+        moved = {"permute_layout": 2 * q_bytes + 2 * kv_bytes,
+                 "permute_ulysses": 2 * q_bytes + 2 * kv_bytes}
+    for k, mv in moved.items():
+        if k in kernels:
+            per_launch = 2 * mv / kernels[k]["launches_per_step"]
+            gbs = per_launch / (kernels[k]["avg_ms"] * 1e-3) / 1e9
+            kernels[k].update({"bytes_per_launch": per_launch, "GB_s": gbs,
+                               "frac_hbm": gbs / pk["hbm_gbs"]})
+
+    # standalone merge on its own workload (4 partials of B*S*Hq rows)
+    merge_res = None
+    try:
+        rows = (1 if w.varlen else w.B) * w.S * w.Hq
+        n = max(2, min(w.cp, 8))
+        g = torch.Generator(device=dev).manual_seed(7)
+        op = torch.randn(n, rows, w.D, device=dev, generator=g)
+        lp = torch.randn(n, rows, device=dev, generator=g)
+        oo = torch.empty(rows, w.D, dtype=torch.bfloat16, device=dev)
+        lo = torch.empty(rows, device=dev)
+        for tree in (0, 1):
+            fn = lambda: usp.usp_merge_partials(op, lp, n, rows, w.D, tree, oo, torch.bfloat16, lo)  # noqa: E731
+            for _ in range(3):
+                fn()
+            mms = timed(fn, 10)
+            by = n * rows * (4 * w.D + 4) + rows * (2 * w.D + 4)
+            gbs = by / (mms * 1e-3) / 1e9
+            merge_res = merge_res or {}
+            merge_res["tree" if tree else "linear"] = {
+                "n": n, "rows": rows, "D": w.D, "ms": mms, "bytes": by, "GB_s": gbs,
+                "frac_hbm": gbs / pk["hbm_gbs"]}
+        del op, lp
+    except Exception as e:  # report, do not hide
+        merge_res = {"error": repr(e)}
+
+    # end to end: pinned host inputs in, results back to pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        host = {n: x[n].cpu().pin_memory() for n in names}
+        outs_host = None
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+
+        def e2e_step():
+            nonlocal outs_host
+            inp = {n: host[n].to(dev, non_blocking=True) for n in names}
+            outs = step(inp)
+            if outs_host is None:
+                outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+            for hb, o in zip(outs_host, outs):
+                hb.copy_(o, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        ems = timed(e2e_step, max(3, min(args.steps, 10)))
+        d2h = sum(t.numel() * t.element_size() for t in outs_host)
+        e2e = {"value": F["total"] * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, desc, thr = oracle_sample(w, args.seed, 20.0)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": desc, "seconds": dt}
+
+    value = F["total"] * world / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "D": w.D, "layout": w.layout, "cp": w.cp, "ulysses": w.ud,
+                   "causal": w.causal, "window": w.window, "sink_tokens": w.sink_tokens,
+                   "backward": w.backward,
+                   "useful_tflop_per_step": F["total"] / 1e12,
+                   "parallelism": f"virtual ring cp={w.cp} x ulysses {w.ud} on one GPU; "
+                                  f"{world} replica(s)",
+                   "l2": "no flush: step inputs larger than L2"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches * args.steps), "clocks": clocks,
+        "kernels": kernels, "merge": merge_res,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

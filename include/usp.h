@@ -1,0 +1,264 @@
+/*
+ * usp.h - C ABI of the GB300 sequence-parallel attention core.
+ *
+ * What the library computes
+ * -------------------------
+ * Exact softmax attention of every query shard against the KV shards of a
+ * ring, in ring order, with the per-shard partials (O, LSE) merged by the
+ * associative log-sum-exp rule so the result equals full attention
+ * ("Long Context Attention" notes, sections "Ring Attention" and "Tree
+ * Attention"; YunChang README, "2. Usage"; ring-sliding-window-attention
+ * README, "Arguments"). cp_size ring ranks and ulysses_degree Ulysses ranks
+ * are virtual: all of them live in one device's memory, the ring hop is an
+ * address offset and the Ulysses all-to-all is a device-memory permute.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *    stated otherwise; the library never frees or retains it after the call
+ *    returns, and allocates no device memory. Scratch space comes from a
+ *    caller-provided workspace whose size the *_workspace_size calls give.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and never synchronises the host. Argument errors are detected
+ *    on the host before anything is launched; the call then returns an error
+ *    status and enqueues no work.
+ *  - Tensor pointers must be 16-byte aligned (USP_ERR_ALIGNMENT otherwise).
+ *  - Tensors are row-major with the layouts stated per call. "Permuted" or
+ *    "rank-major" sequence order means the concatenation of ring rank 0's
+ *    shard, rank 1's shard, ..., each shard in increasing natural position:
+ *      contiguous: rank r holds positions [r*S/cp, (r+1)*S/cp)
+ *      zigzag:     S is cut into 2*cp chunks of S/(2*cp); rank r holds chunk
+ *                  r then chunk 2*cp-1-r ("Zig-Zag Attention": folding the
+ *                  causal mask makes every cross-rank chunk pair a full
+ *                  square or empty and balances the work)
+ *      stripe:     rank r holds positions r, r+cp, r+2cp, ... ("Solution":
+ *                  KV0 holds tokens 0,4,8,12 of 16 on 4 hosts)
+ *  - With ulysses_degree ud > 1 the world is W = cp*ud ranks numbered
+ *    w = rho*ud + u (rho = ring rank, u = Ulysses rank). Rank w's sequence
+ *    shard is permuted positions [w*S/W, (w+1)*S/W).
+ *
+ * Masks. Query position i sees key position j (positions counted from the
+ * start of their own sequence; keys of another packed sequence are never
+ * visible) iff
+ *     (!causal || j <= i) && (window <= 0 || i - j < window || j < sink_tokens)
+ * `window` is the number of visible keys including the query itself
+ * (ring-sliding-window README, "Arguments": window_size); `sink_tokens`
+ * leading tokens of every sequence stay visible outside the window (the
+ * README's "Ring Streaming LLM Attention"). A query that sees no key gets
+ * O = 0 and LSE = -inf.
+ */
+#ifndef USP_H_
+#define USP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *usp_stream_t;
+
+typedef enum {
+  USP_OK = 0,
+  USP_ERR_INVALID_ARG = 1,  /* a size, degree, enum or pointer is invalid   */
+  USP_ERR_UNSUPPORTED = 2,  /* valid, but this build has no kernel for it   */
+  USP_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned             */
+  USP_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required   */
+  USP_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, attrs)   */
+  USP_ERR_TIMEOUT = 6       /* a device wait gave up (reported by a kernel) */
+} usp_status_t;
+
+typedef enum {
+  USP_LAYOUT_CONTIGUOUS = 0,
+  USP_LAYOUT_ZIGZAG = 1,
+  USP_LAYOUT_STRIPE = 2
+} usp_layout_t;
+
+typedef enum { USP_BF16 = 0, USP_FP32 = 1 } usp_dtype_t;
+
+typedef enum {
+  USP_PERMUTE_EXTRACT = 0,          /* natural order -> rank-major order  */
+  USP_PERMUTE_RESTORE = 1,          /* rank-major order -> natural order  */
+  USP_PERMUTE_ULYSSES_SEQ2HEAD = 2, /* Ulysses all-to-all before attention */
+  USP_PERMUTE_ULYSSES_HEAD2SEQ = 3  /* Ulysses all-to-all after attention  */
+} usp_permute_kind_t;
+
+/* Flags for the attention calls. */
+#define USP_FLAG_NONE 0u
+/* Run the CUDA-core fp32 kernels even where the tensor-core kernels apply
+ * (bf16 inputs). Used to cross-check the two kernel families. */
+#define USP_FLAG_FORCE_SIMT 1u
+
+/*
+ * usp_attn_fwd - ring attention forward with the fused LSE merge.
+ *
+ * Defines: per ring rank rho and step s = 0..cp-1, the partial attention of
+ * rho's queries against the KV shard of rank (rho - s) mod cp ("Ring
+ * Attention": KV segments circulate until every host has seen all of them),
+ * merged in step order with the log-sum-exp rule ("Tree Attention":
+ * logsumexp and max are associative). The merged running partial is kept
+ * unnormalised (row max m, row sum l, sum of exp-weighted values) inside the
+ * kernel; that representation is equivalent to (O = acc/l, LSE = m + log l).
+ * With ulysses_degree > 1 (USP), q/k/v are first exchanged sequence->head
+ * inside the workspace, each Ulysses group runs its ring over its H/ud
+ * heads, and the output is exchanged head->sequence back into `out`.
+ *
+ * q    [B, S, Hq, D]   (packed: [S, Hq, D], S = total tokens T), rank-major
+ * k, v [B, S, Hkv, D]  (packed: [S, Hkv, D]), rank-major, same layout as q
+ * out  [B, S, Hq, D]   written, rank-major, dtype as q
+ * lse  [B, Hq, S] fp32 written (packed: [Hq, S]), natural log of the scaled
+ *      scores' sum of exponentials, rank-major sequence order
+ * B, S, Hq, Hkv, D   D in {64, 128}; Hq % Hkv == 0 (query head h reads KV
+ *      head h / (Hq/Hkv)); Hq % ud == 0 and Hkv % ud == 0 (Ulysses splits
+ *      heads, YunChang README "Why not apply Ulysses ... individually");
+ *      S % (cp*ud) == 0, zigzag also S % (2*cp*ud) == 0.
+ * softmax_scale  <= 0 selects 1/sqrt(D) (the README's default).
+ * causal, window, sink_tokens  the mask above. sink_tokens >= 0.
+ * cu_seqlens  NULL for dense batches. Otherwise int32 [B + 1] device array
+ *      of cumulative sequence lengths over the whole packed batch and all
+ *      ranks (ring-sliding-window README, "Arguments": cu_seqlens is global,
+ *      not per rank), cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = S;
+ *      B is then the number of sequences and the layout applies to the
+ *      packed sequence. The values are trusted (not checked on the device):
+ *      malformed boundaries give wrong masks but no out-of-bounds access.
+ * cp_size >= 1, ulysses_degree >= 1, layout, dtype (q/k/v/out element type).
+ * flags  USP_FLAG_*.
+ * workspace / workspace_bytes  caller scratch of at least
+ *      usp_attn_fwd_workspace_size(...) bytes, 256-byte aligned (may be NULL
+ *      when that size is 0). Its contents on entry are irrelevant.
+ * Errors: USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, USP_ERR_WORKSPACE,
+ *      USP_ERR_UNSUPPORTED (fp32 with D not in {64,128}), USP_ERR_CUDA.
+ */
+usp_status_t usp_attn_fwd(const void *q, const void *k, const void *v,
+                          void *out, float *lse, int B, int S, int Hq, int Hkv,
+                          int D, float softmax_scale, int causal, int window,
+                          int sink_tokens, const int32_t *cu_seqlens,
+                          int cp_size, int ulysses_degree, usp_layout_t layout,
+                          usp_dtype_t dtype, unsigned flags, void *workspace,
+                          size_t workspace_bytes, usp_stream_t stream);
+
+size_t usp_attn_fwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
+                                   int cp_size, int ulysses_degree,
+                                   usp_dtype_t dtype, unsigned flags);
+
+/*
+ * usp_attn_bwd - gradients of usp_attn_fwd from the saved (out, lse).
+ *
+ * The LSE kept by the forward pass is what the backward pass needs ("Long
+ * Context Attention" notes, "Motivation": QKV, output, LSE and dout are
+ * stored for the backward). With P = exp(scale*q.k - LSE):
+ *   Delta_i = <dO_i, O_i>, dV = P^T dO, dS = P * (dO V^T - Delta),
+ *   dQ = scale dS K, dK = scale dS^T Q,
+ * accumulated over every ring step; dK/dV of a shard collect the
+ * contributions of every query rank that saw it (the shard's ring return)
+ * and of all Hq/Hkv query heads sharing the KV head.
+ *
+ * q, k, v, out, lse: as passed to / produced by usp_attn_fwd (same args).
+ * dout [B,S,Hq,D] rank-major, dtype as q. dq/dk/dv written, shapes of q/k/v.
+ * Scalar arguments must equal those of the forward call.
+ * Errors: as usp_attn_fwd.
+ */
+usp_status_t usp_attn_bwd(const void *q, const void *k, const void *v,
+                          const void *out, const float *lse, const void *dout,
+                          void *dq, void *dk, void *dv, int B, int S, int Hq,
+                          int Hkv, int D, float softmax_scale, int causal,
+                          int window, int sink_tokens,
+                          const int32_t *cu_seqlens, int cp_size,
+                          int ulysses_degree, usp_layout_t layout,
+                          usp_dtype_t dtype, unsigned flags, void *workspace,
+                          size_t workspace_bytes, usp_stream_t stream);
+
+size_t usp_attn_bwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
+                                   int cp_size, int ulysses_degree,
+                                   usp_dtype_t dtype, unsigned flags);
+
+/*
+ * usp_merge_partials - merge n attention partials with the log-sum-exp rule.
+ *
+ * "Tree Attention" (Long Context Attention notes): because logsumexp and max
+ * are associative, partials over disjoint key sets can be reduced in any
+ * order, e.g. a tree. For two partials
+ *   L = max + log(exp(L_a - max) + exp(L_b - max)),
+ *   O = exp(L_a - L) O_a + exp(L_b - L) O_b;
+ * a partial with L = -inf is the identity (its O is ignored).
+ *
+ * o_parts   [n, rows, D] fp32, lse_parts [n, rows] fp32 (partial i at i*rows)
+ * n >= 1 (tree_order: n <= 64), rows >= 0, D in {64, 128}
+ * tree_order 0: ((p0 + p1) + p2) + ...   (ring order)
+ *            1: pairwise levels (p0+p1), (p2+p3), ...; an odd last partial
+ *               moves up a level unchanged.
+ * o_out [rows, D] written in out_dtype; lse_out [rows] fp32 written.
+ * Errors: USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, USP_ERR_CUDA.
+ */
+usp_status_t usp_merge_partials(const float *o_parts, const float *lse_parts,
+                                int n, int64_t rows, int D, int tree_order,
+                                void *o_out, usp_dtype_t out_dtype,
+                                float *lse_out, usp_stream_t stream);
+
+/*
+ * usp_permute - sequence layouts and the Ulysses all-to-all, bit-exact.
+ *
+ * EXTRACT / RESTORE (the YunChang README's EXTRACT_FUNC_DICT /
+ * zigzag_extract_local reorder, "2. Usage"; stripe and zigzag as in the
+ * conventions above):
+ *   src/dst [B, S, H, D] (packed: B = 1 and S = T; pass cu_seqlens = NULL,
+ *   the layout applies to the packed sequence as a whole).
+ *   EXTRACT: dst[b][p] = src[b][pos(p)], RESTORE: dst[b][pos(p)] = src[b][p].
+ * ULYSSES_SEQ2HEAD (DeepSpeed-Ulysses exchange inside USP; the degree cannot
+ *   exceed the head count, YunChang README): rank w = rho*ud + u sends the
+ *   head slice u' of its sequence shard to rank (rho, u'), which stacks the
+ *   slices it receives along the sequence in u order. Emulated layout:
+ *     src [B, S, H, D] rank-major -> dst [ud, B, S, H/ud, D] with
+ *     dst[u][b][p][h][d] = src[b][p][u*H/ud + h][d].
+ * ULYSSES_HEAD2SEQ is its inverse (dst [B,S,H,D], src [ud,B,S,H/ud,D]).
+ * elem_bytes 2 or 4. H*D*elem_bytes (Ulysses: H/ud*D*elem_bytes) must be a
+ * multiple of 16. S divisible as for usp_attn_fwd. src and dst must not
+ * overlap. Errors: USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, USP_ERR_CUDA.
+ */
+usp_status_t usp_permute(const void *src, void *dst, usp_permute_kind_t kind,
+                         usp_layout_t layout, int B, int S, int H, int D,
+                         int cp_size, int ulysses_degree, int elem_bytes,
+                         usp_stream_t stream);
+
+/*
+ * Kernel timer, for benchmarks and profiling (no counterpart on the pages).
+ * While enabled, every kernel this library launches is bracketed by a pair
+ * of CUDA events recorded on the launch stream. usp_profile_read() waits
+ * for the recorded events, writes one entry per kernel name (launch count
+ * and summed device milliseconds) into `stats` (at most max_stats entries),
+ * clears the records and returns the number of entries written (negative
+ * on a CUDA error). Not thread-safe: enable it only in single-threaded
+ * measurement code. The events are created by the CUDA runtime; no device
+ * memory is allocated.
+ */
+typedef struct {
+  char name[48];
+  uint64_t launches;
+  double total_ms;
+} usp_kernel_stat_t;
+
+usp_status_t usp_profile_enable(int on);
+int usp_profile_read(usp_kernel_stat_t *stats, int max_stats);
+
+/* Waits for the device, then reports (and clears) what the kernels flagged
+ * since the last call: USP_ERR_TIMEOUT if a tensor-core kernel gave up on a
+ * pipeline wait (each wait is bounded; a kernel that gives up skips its
+ * remaining work, frees its tensor memory and exits, leaving its outputs
+ * unspecified), USP_ERR_CUDA if the device reports an error, else USP_OK.
+ * Synchronises the whole device: a diagnostics call, not for hot loops. */
+usp_status_t usp_device_status(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *usp_status_string(usp_status_t status);
+
+/* Number of kernel launches this library has enqueued in the calling
+ * process so far (host-side counter; for launch accounting). */
+uint64_t usp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USP_H_ */

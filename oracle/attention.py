@@ -229,3 +229,78 @@ def count_visible_pairs(S: int, causal: bool, window: int, sink_tokens: int,
             total += int(visibility(pos[r0:r1], pos, causal, window,
                                     sink_tokens).sum())
     return total
+
+
+def attn_bwd_sampled(q, k, v, dout, scale: float, b: int, g: int,
+                     q_rows: Iterable[int], k_rows: Iterable[int],
+                     causal: bool = True, window: int = 0, sink_tokens: int = 0,
+                     cu_seqlens=None, block: int = 2048):
+    """Gradient rows for spot checks at full problem size.
+
+    Returns (dq [G, nq, D] for q_rows of every query head of KV group g,
+    dk [nk, D], dv [nk, D] for k_rows of KV head g), batch b (packed: b=0).
+    Uses the identity sum_j P_ij dP_ij = <dO_i, O_i> (the P row sums to one),
+    with O and LSE from this module's own forward of the group's heads.
+    """
+    packed = cu_seqlens is not None
+    sel = (lambda t: t) if packed else (lambda t: t[b])
+    G = q.shape[-2] // k.shape[-2]
+    heads = list(range(g * G, (g + 1) * G))
+    # only the group's heads are converted (inputs can be several GB)
+    qb = np.stack([_f64(sel(q)[:, h]) for h in heads], axis=1)
+    dob = np.stack([_f64(sel(dout)[:, h]) for h in heads], axis=1)
+    kk, vv = _f64(sel(k)[:, g]), _f64(sel(v)[:, g])
+    S, _, D = qb.shape
+    segs = _segments(S, cu_seqlens)
+    starts = np.array([s for s, _ in segs])
+    # full forward (O, LSE) of the group's heads, segment by segment; heads
+    # are independent and run on threads (NumPy releases the GIL).
+    O = np.zeros((G, S, D))
+    L = np.zeros((G, S))
+
+    def head_fwd(hi):
+        for (a, e) in segs:
+            pos = np.arange(e - a)
+            for r0 in range(0, e - a, block):
+                r1 = min(e - a, r0 + block)
+                kend = r1 if causal else e - a
+                vis = visibility(pos[r0:r1], pos[:kend], causal, window,
+                                 sink_tokens)
+                o, lse = softmax_rows(qb[a + r0:a + r1, hi], kk[a:a + kend],
+                                      vv[a:a + kend], vis, scale)
+                O[hi, a + r0:a + r1] = o
+                L[hi, a + r0:a + r1] = lse
+
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=G) as ex:
+        list(ex.map(head_fwd, range(G)))
+    delta = np.einsum("hsd,shd->hs", O, dob)
+    q_rows = [int(r) for r in q_rows]
+    k_rows = [int(r) for r in k_rows]
+    dq = np.zeros((G, len(q_rows), D))
+    for n, r in enumerate(q_rows):
+        si = int(np.searchsorted(starts, r, side="right") - 1)
+        a, e = segs[si]
+        vis = visibility(np.array([r - a]), np.arange(e - a), causal, window,
+                         sink_tokens)[0]
+        js = a + np.nonzero(vis)[0]
+        for hi in range(G):
+            s = scale * (kk[js] @ qb[r, hi])
+            P = np.exp(s - L[hi, r])
+            dS = P * (vv[js] @ dob[r, hi] - delta[hi, r])
+            dq[hi, n] = scale * (dS @ kk[js])
+    dk = np.zeros((len(k_rows), D))
+    dv = np.zeros((len(k_rows), D))
+    for n, j in enumerate(k_rows):
+        si = int(np.searchsorted(starts, j, side="right") - 1)
+        a, e = segs[si]
+        vis = visibility(np.arange(e - a), np.array([j - a]), causal, window,
+                         sink_tokens)[:, 0]
+        iis = a + np.nonzero(vis)[0]
+        for hi in range(G):
+            s = scale * (qb[iis, hi] @ kk[j])
+            P = np.exp(s - L[hi, iis])
+            dS = P * (dob[iis, hi] @ vv[j] - delta[hi, iis])
+            dv[n] += P @ dob[iis, hi]
+            dk[n] += scale * (dS @ qb[iis, hi])
+    return dq, dk, dv

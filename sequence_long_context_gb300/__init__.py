@@ -1,0 +1,202 @@
+"""GB300-native sequence-parallel attention core (Python binding).
+
+The functions named usp_* mirror the C ABI of include/usp.h one to one and
+only marshal arguments (tensors -> device pointers, the current CUDA stream).
+Every step of the computation runs in the CUDA library libusp.so; there is
+no Python or CPU fallback, and a missing library raises.
+
+The helpers below them (attn_forward, attn_backward, permute,
+merge_partials) allocate outputs and workspaces with PyTorch and call the
+same entry points.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+LAYOUT = {"contiguous": 0, "zigzag": 1, "stripe": 2}
+DTYPE = {torch.bfloat16: 0, torch.float32: 1}
+PERMUTE = {"extract": 0, "restore": 1, "seq2head": 2, "head2seq": 3}
+FLAG_FORCE_SIMT = 1
+
+
+class UspError(RuntimeError):
+    pass
+
+
+def _p(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr() if x.numel() else None
+    return int(x)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        name = _lib.load().usp_status_string(status).decode()
+        raise UspError(name)
+
+
+def _enum(table, x) -> int:
+    return table[x] if not isinstance(x, int) else x
+
+
+# --- the C ABI, one to one ---------------------------------------------------
+
+def usp_attn_fwd(q, k, v, out, lse, B, S, Hq, Hkv, D, softmax_scale, causal,
+                 window, sink_tokens, cu_seqlens, cp_size, ulysses_degree,
+                 layout, dtype, flags=0, workspace=None, workspace_bytes=0,
+                 stream=None) -> None:
+    _check(_lib.load().usp_attn_fwd(
+        _p(q), _p(k), _p(v), _p(out), _p(lse), B, S, Hq, Hkv, D,
+        float(softmax_scale), int(causal), int(window), int(sink_tokens),
+        _p(cu_seqlens), cp_size, ulysses_degree, _enum(LAYOUT, layout),
+        _enum(DTYPE, dtype), flags, _p(workspace), int(workspace_bytes),
+        _stream(stream)))
+
+
+def usp_attn_fwd_workspace_size(B, S, Hq, Hkv, D, cp_size, ulysses_degree,
+                                dtype, flags=0) -> int:
+    return int(_lib.load().usp_attn_fwd_workspace_size(
+        B, S, Hq, Hkv, D, cp_size, ulysses_degree, _enum(DTYPE, dtype), flags))
+
+
+def usp_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D,
+                 softmax_scale, causal, window, sink_tokens, cu_seqlens,
+                 cp_size, ulysses_degree, layout, dtype, flags=0,
+                 workspace=None, workspace_bytes=0, stream=None) -> None:
+    _check(_lib.load().usp_attn_bwd(
+        _p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk),
+        _p(dv), B, S, Hq, Hkv, D, float(softmax_scale), int(causal),
+        int(window), int(sink_tokens), _p(cu_seqlens), cp_size,
+        ulysses_degree, _enum(LAYOUT, layout), _enum(DTYPE, dtype), flags,
+        _p(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def usp_attn_bwd_workspace_size(B, S, Hq, Hkv, D, cp_size, ulysses_degree,
+                                dtype, flags=0) -> int:
+    return int(_lib.load().usp_attn_bwd_workspace_size(
+        B, S, Hq, Hkv, D, cp_size, ulysses_degree, _enum(DTYPE, dtype), flags))
+
+
+def usp_merge_partials(o_parts, lse_parts, n, rows, D, tree_order, o_out,
+                       out_dtype, lse_out, stream=None) -> None:
+    _check(_lib.load().usp_merge_partials(
+        _p(o_parts), _p(lse_parts), n, rows, D, int(tree_order), _p(o_out),
+        _enum(DTYPE, out_dtype), _p(lse_out), _stream(stream)))
+
+
+def usp_permute(src, dst, kind, layout, B, S, H, D, cp_size, ulysses_degree,
+                elem_bytes, stream=None) -> None:
+    _check(_lib.load().usp_permute(
+        _p(src), _p(dst), _enum(PERMUTE, kind), _enum(LAYOUT, layout), B, S, H,
+        D, cp_size, ulysses_degree, elem_bytes, _stream(stream)))
+
+
+def usp_launch_count() -> int:
+    return int(_lib.load().usp_launch_count())
+
+
+def usp_device_status() -> None:
+    """Raise if a kernel flagged a failed (timed-out) wait since the last call."""
+    _check(_lib.load().usp_device_status())
+
+
+def usp_profile_enable(on: bool) -> None:
+    _check(_lib.load().usp_profile_enable(int(bool(on))))
+
+
+def usp_profile_read(max_stats: int = 64) -> dict:
+    """{kernel name: (launches, total device ms)} since the last read."""
+    arr = (_lib.KernelStat * max_stats)()
+    n = _lib.load().usp_profile_read(arr, max_stats)
+    if n < 0:
+        raise UspError("USP_ERR_CUDA")
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(n)}
+
+
+# --- allocation helpers -----------------------------------------------------
+
+def _dims(q: torch.Tensor, k: torch.Tensor, cu_seqlens):
+    if cu_seqlens is not None:
+        T, Hq, D = q.shape
+        return int(cu_seqlens.numel() - 1), T, Hq, k.shape[1], D, 1
+    B, S, Hq, D = q.shape
+    return B, S, Hq, k.shape[2], D, B
+
+
+def attn_forward(q, k, v, *, causal=True, window=0, sink_tokens=0,
+                 cu_seqlens=None, cp=1, ud=1, layout="contiguous",
+                 softmax_scale=0.0, flags=0, stream=None
+                 ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(out, lse) for rank-major q/k/v ([B,S,H,D] or packed [T,H,D])."""
+    B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
+    out = torch.empty_like(q)
+    lse = torch.empty((Bl, Hq, S) if cu_seqlens is None else (Hq, S),
+                      dtype=torch.float32, device=q.device)
+    ws_n = usp_attn_fwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=q.device) if ws_n else None
+    usp_attn_fwd(q, k, v, out, lse, B, S, Hq, Hkv, D, softmax_scale, causal,
+                 window, sink_tokens, cu_seqlens, cp, ud, layout, q.dtype,
+                 flags, ws, ws_n, stream)
+    return out, lse
+
+
+def attn_backward(q, k, v, out, lse, dout, *, causal=True, window=0,
+                  sink_tokens=0, cu_seqlens=None, cp=1, ud=1,
+                  layout="contiguous", softmax_scale=0.0, flags=0,
+                  stream=None):
+    """(dq, dk, dv) for rank-major tensors and the forward's (out, lse)."""
+    B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_n = usp_attn_bwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=q.device)
+    usp_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D,
+                 softmax_scale, causal, window, sink_tokens, cu_seqlens, cp,
+                 ud, layout, q.dtype, flags, ws, ws_n, stream)
+    return dq, dk, dv
+
+
+def permute(x: torch.Tensor, kind: str, layout: str = "contiguous", cp: int = 1,
+            ud: int = 1, stream=None) -> torch.Tensor:
+    """Layout extract/restore of [B,S,H,D] (packed: [T,H,D]) or the Ulysses
+    exchange ([B,S,H,D] <-> [ud,B,S,H/ud,D])."""
+    if kind in ("extract", "restore"):
+        xb = x if x.dim() == 4 else x.unsqueeze(0)
+        B, S, H, D = xb.shape
+        dst = torch.empty_like(x)
+    elif kind == "seq2head":
+        B, S, H, D = x.shape
+        dst = torch.empty((ud, B, S, H // ud, D), dtype=x.dtype, device=x.device)
+    else:
+        _, B, S, Hg, D = x.shape
+        H = Hg * ud
+        dst = torch.empty((B, S, H, D), dtype=x.dtype, device=x.device)
+    usp_permute(x, dst, kind, layout, B, S, H, D, cp, ud, x.element_size(),
+                stream)
+    return dst
+
+
+def merge_partials(o_parts: torch.Tensor, lse_parts: torch.Tensor,
+                   tree_order: bool = False, out_dtype=torch.float32,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """o_parts [n, rows, D] fp32, lse_parts [n, rows] -> (O [rows, D], LSE)."""
+    n, rows, D = o_parts.shape
+    o = torch.empty((rows, D), dtype=out_dtype, device=o_parts.device)
+    lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+    usp_merge_partials(o_parts, lse_parts, n, rows, D, tree_order, o,
+                       out_dtype, lse, stream)
+    return o, lse

@@ -1,0 +1,428 @@
+// C ABI entry points: argument validation, workspace carving, dispatch.
+//
+// Every check happens on the host before any launch, so a call that returns
+// an error has enqueued nothing. The library allocates no device memory;
+// scratch is carved out of the caller's workspace in 256-byte aligned slices.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace usp {
+
+static std::atomic<unsigned long long> g_launches{0};
+
+namespace {
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+ProfScope::ProfScope(cudaStream_t s, const char* name) : idx(-1), st(s) {
+  if (!g_prof_on) return;
+  ProfRec r{name, prof_event(), prof_event()};
+  if (!r.a || !r.b) return;
+  cudaEventRecord(r.a, st);
+  g_prof_recs.push_back(r);
+  idx = (int)g_prof_recs.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (idx >= 0) cudaEventRecord(g_prof_recs[idx].b, st);
+}
+
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n); }
+
+usp_status_t check_launch() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? USP_OK : USP_ERR_CUDA;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+struct Shape {
+  int B, S, Hq, Hkv, D, cp, ud, layout, dtype, varlen;
+  size_t elem() const { return dtype == USP_FP32 ? 4 : 2; }
+  size_t q_bytes() const { return (size_t)B_eff() * S * Hq * D * elem(); }
+  size_t kv_bytes() const { return (size_t)B_eff() * S * Hkv * D * elem(); }
+  int B_eff() const { return varlen ? 1 : B; }
+};
+
+usp_status_t validate(const Shape& s, int window, int sink) {
+  if (s.B < 0 || s.S < 0 || s.Hq <= 0 || s.Hkv <= 0) return USP_ERR_INVALID_ARG;
+  if (s.varlen && s.B < 1) return USP_ERR_INVALID_ARG;
+  if (s.D != 64 && s.D != 128) return USP_ERR_UNSUPPORTED;
+  if (s.Hq % s.Hkv != 0) return USP_ERR_INVALID_ARG;
+  if (s.cp < 1 || s.ud < 1) return USP_ERR_INVALID_ARG;
+  if (s.Hq % s.ud != 0 || s.Hkv % s.ud != 0) return USP_ERR_INVALID_ARG;
+  if (s.layout < USP_LAYOUT_CONTIGUOUS || s.layout > USP_LAYOUT_STRIPE)
+    return USP_ERR_INVALID_ARG;
+  if (s.dtype != USP_BF16 && s.dtype != USP_FP32) return USP_ERR_INVALID_ARG;
+  int div = s.cp * s.ud * (s.layout == USP_LAYOUT_ZIGZAG ? 2 : 1);
+  if (s.S % div != 0) return USP_ERR_INVALID_ARG;
+  if (sink < 0) return USP_ERR_INVALID_ARG;
+  (void)window;
+  // 32-bit element offsets inside the copy kernels and grid limits
+  if ((double)s.B_eff() * s.S * s.Hq * s.D >= 2147483647.0 * 8.0)
+    return USP_ERR_UNSUPPORTED;
+  if ((long long)s.B_eff() * s.ud > 65535 || s.Hq > 65535)
+    return USP_ERR_UNSUPPORTED;
+  return USP_OK;
+}
+
+AttnParams make_params(const Shape& s, float scale, int causal, int window,
+                       int sink, const int32_t* cu) {
+  AttnParams P{};
+  P.B = s.B_eff();
+  P.ud = s.ud;
+  P.Bt = P.B * s.ud;
+  P.S = s.S;
+  P.Hq = s.Hq / s.ud;
+  P.Hkv = s.Hkv / s.ud;
+  P.D = s.D;
+  P.G = s.Hq / s.Hkv;
+  // LSE [B][Hq_total][S]: u-th group's head h is global head u*Hq/ud + h
+  P.lse_sh = s.S;
+  P.lse_su = (long long)P.Hq * s.S;
+  P.lse_sb = (long long)s.Hq * s.S;
+  P.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)s.D);
+  P.scale_log2 = P.scale * 1.4426950408889634f;
+  P.causal = causal ? 1 : 0;
+  P.window = window > 0 ? window : 0;
+  P.sink = sink;
+  P.cu = cu;
+  P.nseq = cu ? s.B : 0;
+  P.cp = s.cp;
+  P.layout = s.layout;
+  P.shard = s.S / s.cp;
+  P.chunk = s.layout == USP_LAYOUT_ZIGZAG ? s.S / (2 * s.cp) : P.shard;
+  return P;
+}
+
+struct Carve {
+  char* base;
+  size_t used = 0;
+  explicit Carve(void* b) : base(static_cast<char*>(b)) {}
+  void* take(size_t bytes) {
+    void* p = base ? base + used : nullptr;
+    used += round_up(bytes);
+    return p;
+  }
+};
+
+// Workspace slices, in order. Only the sizes matter when base == nullptr.
+struct FwdWs {
+  void *q, *k, *v, *o;
+};
+FwdWs carve_fwd(Carve& c, const Shape& s) {
+  FwdWs w{};
+  if (s.ud > 1) {
+    w.q = c.take(s.q_bytes());
+    w.k = c.take(s.kv_bytes());
+    w.v = c.take(s.kv_bytes());
+    w.o = c.take(s.q_bytes());
+  }
+  return w;
+}
+
+struct BwdWs {
+  float* delta;
+  float* dq_acc;
+  void *q, *k, *v, *o, *dout, *dq, *dk, *dv;
+};
+BwdWs carve_bwd(Carve& c, const Shape& s, bool tc) {
+  BwdWs w{};
+  w.delta = static_cast<float*>(c.take((size_t)s.B_eff() * s.Hq * s.S * 4));
+  if (tc) w.dq_acc = static_cast<float*>(c.take((size_t)s.B_eff() * s.S * s.Hq * s.D * 4));
+  if (s.ud > 1) {
+    w.q = c.take(s.q_bytes());
+    w.k = c.take(s.kv_bytes());
+    w.v = c.take(s.kv_bytes());
+    w.o = c.take(s.q_bytes());
+    w.dout = c.take(s.q_bytes());
+    w.dq = c.take(s.q_bytes());
+    w.dk = c.take(s.kv_bytes());
+    w.dv = c.take(s.kv_bytes());
+  }
+  return w;
+}
+
+Shape shape_of(int B, int S, int Hq, int Hkv, int D, int cp, int ud,
+               int layout, int dtype, int varlen) {
+  Shape s{B, S, Hq, Hkv, D, cp, ud, layout, dtype, varlen};
+  return s;
+}
+
+bool use_tc_fwd(const AttnParams& P, const Shape& s, unsigned flags) {
+  return s.dtype == USP_BF16 && !(flags & USP_FLAG_FORCE_SIMT) &&
+         fwd_tc_supported(P);
+}
+bool use_tc_bwd(const AttnParams& P, const Shape& s, unsigned flags) {
+  return s.dtype == USP_BF16 && !(flags & USP_FLAG_FORCE_SIMT) &&
+         bwd_tc_supported(P);
+}
+
+// Ulysses exchange of one [B,S,H,D] tensor (row = H*D*elem bytes).
+usp_status_t a2a(const void* src, void* dst, const Shape& s, int H, int s2h,
+                 cudaStream_t st) {
+  return launch_ulysses(src, dst, s.B_eff(), s.S, (int)(H * s.D * s.elem()),
+                        s.ud, s2h, st);
+}
+
+}  // namespace
+}  // namespace usp
+
+using namespace usp;
+
+extern "C" {
+
+const char* usp_status_string(usp_status_t st) {
+  switch (st) {
+    case USP_OK: return "USP_OK";
+    case USP_ERR_INVALID_ARG: return "USP_ERR_INVALID_ARG";
+    case USP_ERR_UNSUPPORTED: return "USP_ERR_UNSUPPORTED";
+    case USP_ERR_ALIGNMENT: return "USP_ERR_ALIGNMENT";
+    case USP_ERR_WORKSPACE: return "USP_ERR_WORKSPACE";
+    case USP_ERR_CUDA: return "USP_ERR_CUDA";
+    case USP_ERR_TIMEOUT: return "USP_ERR_TIMEOUT";
+  }
+  return "USP_ERR_UNKNOWN";
+}
+
+uint64_t usp_launch_count(void) { return g_launches.load(); }
+
+usp_status_t usp_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return USP_ERR_CUDA;
+  int a = read_clear_fwd_tc_status(), b = read_clear_bwd_tc_status();
+  if (a < 0 || b < 0) return USP_ERR_CUDA;
+  if (a == USP_ERR_TIMEOUT || b == USP_ERR_TIMEOUT) return USP_ERR_TIMEOUT;
+  return USP_OK;
+}
+
+usp_status_t usp_profile_enable(int on) {
+  g_prof_on = on != 0;
+  return USP_OK;
+}
+
+int usp_profile_read(usp_kernel_stat_t* stats, int max_stats) {
+  std::map<std::string, std::pair<uint64_t, double>> agg;
+  int rc = 0;
+  for (ProfRec& r : g_prof_recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      rc = -1;
+    auto& e = agg[r.name];
+    e.first += 1;
+    e.second += ms;
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  if (rc < 0) return rc;
+  int n = 0;
+  for (auto& kv : agg) {
+    if (n >= max_stats || !stats) break;
+    std::memset(stats[n].name, 0, sizeof(stats[n].name));
+    std::strncpy(stats[n].name, kv.first.c_str(), sizeof(stats[n].name) - 1);
+    stats[n].launches = kv.second.first;
+    stats[n].total_ms = kv.second.second;
+    ++n;
+  }
+  return n;
+}
+
+size_t usp_attn_fwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
+                                   int cp, int ud, usp_dtype_t dtype,
+                                   unsigned flags) {
+  (void)flags;
+  Shape s = shape_of(B, S, Hq, Hkv, D, cp, ud, 0, dtype, 0);
+  Carve c(nullptr);
+  carve_fwd(c, s);
+  return c.used;
+}
+
+size_t usp_attn_bwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
+                                   int cp, int ud, usp_dtype_t dtype,
+                                   unsigned flags) {
+  Shape s = shape_of(B, S, Hq, Hkv, D, cp, ud, 0, dtype, 0);
+  Carve c(nullptr);
+  bool tc = dtype == USP_BF16 && !(flags & USP_FLAG_FORCE_SIMT);
+  carve_bwd(c, s, tc);
+  return c.used;
+}
+
+usp_status_t usp_attn_fwd(const void* q, const void* k, const void* v,
+                          void* out, float* lse, int B, int S, int Hq, int Hkv,
+                          int D, float softmax_scale, int causal, int window,
+                          int sink_tokens, const int32_t* cu_seqlens,
+                          int cp_size, int ulysses_degree, usp_layout_t layout,
+                          usp_dtype_t dtype, unsigned flags, void* workspace,
+                          size_t workspace_bytes, usp_stream_t stream) {
+  Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, dtype,
+                     cu_seqlens != nullptr);
+  usp_status_t r = validate(s, window, sink_tokens);
+  if (r != USP_OK) return r;
+  if (S > 0 && (!q || !k || !v || !out || !lse)) return USP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(lse) || !aligned16(workspace))
+    return USP_ERR_ALIGNMENT;
+  if (s.B_eff() == 0 || S == 0) return USP_OK;
+  Carve c(workspace);
+  FwdWs w = carve_fwd(c, s);
+  if (c.used > 0 && (!workspace || workspace_bytes < c.used))
+    return USP_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  AttnParams P = make_params(s, softmax_scale, causal, window, sink_tokens,
+                             cu_seqlens);
+  if (s.ud > 1) {
+    if ((r = a2a(q, w.q, s, Hq, 1, st)) != USP_OK) return r;
+    if ((r = a2a(k, w.k, s, Hkv, 1, st)) != USP_OK) return r;
+    if ((r = a2a(v, w.v, s, Hkv, 1, st)) != USP_OK) return r;
+    P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o;
+  } else {
+    P.q = q; P.k = k; P.v = v; P.o = out;
+  }
+  P.lse = lse;
+  if (use_tc_fwd(P, s, flags))
+    r = launch_fwd_tc(P, st);
+  else
+    r = launch_fwd_simt(P, dtype == USP_BF16, st);
+  if (r != USP_OK) return r;
+  if (s.ud > 1) r = a2a(w.o, out, s, Hq, 0, st);
+  return r;
+}
+
+usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
+                          const void* out, const float* lse, const void* dout,
+                          void* dq, void* dk, void* dv, int B, int S, int Hq,
+                          int Hkv, int D, float softmax_scale, int causal,
+                          int window, int sink_tokens,
+                          const int32_t* cu_seqlens, int cp_size,
+                          int ulysses_degree, usp_layout_t layout,
+                          usp_dtype_t dtype, unsigned flags, void* workspace,
+                          size_t workspace_bytes, usp_stream_t stream) {
+  Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, dtype,
+                     cu_seqlens != nullptr);
+  usp_status_t r = validate(s, window, sink_tokens);
+  if (r != USP_OK) return r;
+  if (S > 0 && (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv))
+    return USP_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return USP_ERR_ALIGNMENT;
+  if (s.B_eff() == 0 || S == 0) return USP_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  AttnParams P = make_params(s, softmax_scale, causal, window, sink_tokens,
+                             cu_seqlens);
+  const bool tc = use_tc_bwd(P, s, flags);
+  Carve c(workspace);
+  BwdWs w = carve_bwd(c, s, tc);
+  if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
+  if (s.ud > 1) {
+    if ((r = a2a(q, w.q, s, Hq, 1, st)) != USP_OK) return r;
+    if ((r = a2a(k, w.k, s, Hkv, 1, st)) != USP_OK) return r;
+    if ((r = a2a(v, w.v, s, Hkv, 1, st)) != USP_OK) return r;
+    if ((r = a2a(out, w.o, s, Hq, 1, st)) != USP_OK) return r;
+    if ((r = a2a(dout, w.dout, s, Hq, 1, st)) != USP_OK) return r;
+    P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o; P.dout = w.dout;
+    P.dq = w.dq; P.dk = w.dk; P.dv = w.dv;
+  } else {
+    P.q = q; P.k = k; P.v = v; P.o = const_cast<void*>(out); P.dout = dout;
+    P.dq = dq; P.dk = dk; P.dv = dv;
+  }
+  P.lse = const_cast<float*>(lse);
+  P.delta = w.delta;
+  P.dq_acc = w.dq_acc;
+  if ((r = launch_bwd_preprocess(P, dtype == USP_BF16, tc ? 1 : 0, st)) != USP_OK)
+    return r;
+  if (tc)
+    r = launch_bwd_tc(P, st);
+  else
+    r = launch_bwd_simt(P, dtype == USP_BF16, st);
+  if (r != USP_OK) return r;
+  if (s.ud > 1) {
+    if ((r = a2a(w.dq, dq, s, Hq, 0, st)) != USP_OK) return r;
+    if ((r = a2a(w.dk, dk, s, Hkv, 0, st)) != USP_OK) return r;
+    if ((r = a2a(w.dv, dv, s, Hkv, 0, st)) != USP_OK) return r;
+  }
+  return USP_OK;
+}
+
+usp_status_t usp_merge_partials(const float* o_parts, const float* lse_parts,
+                                int n, int64_t rows, int D, int tree_order,
+                                void* o_out, usp_dtype_t out_dtype,
+                                float* lse_out, usp_stream_t stream) {
+  if (n < 1 || rows < 0 || (tree_order && n > 64)) return USP_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return USP_ERR_INVALID_ARG;
+  if (out_dtype != USP_BF16 && out_dtype != USP_FP32) return USP_ERR_INVALID_ARG;
+  if (rows > 0 && (!o_parts || !lse_parts || !o_out || !lse_out))
+    return USP_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o_out) ||
+      !aligned16(lse_out))
+    return USP_ERR_ALIGNMENT;
+  return launch_merge(o_parts, lse_parts, n, rows, D, tree_order ? 1 : 0, o_out,
+                      out_dtype == USP_BF16 ? 1 : 0, lse_out,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+usp_status_t usp_permute(const void* src, void* dst, usp_permute_kind_t kind,
+                         usp_layout_t layout, int B, int S, int H, int D,
+                         int cp_size, int ulysses_degree, int elem_bytes,
+                         usp_stream_t stream) {
+  if (B < 0 || S < 0 || H <= 0 || D <= 0 || cp_size < 1 || ulysses_degree < 1)
+    return USP_ERR_INVALID_ARG;
+  if (elem_bytes != 2 && elem_bytes != 4) return USP_ERR_INVALID_ARG;
+  if (layout < USP_LAYOUT_CONTIGUOUS || layout > USP_LAYOUT_STRIPE)
+    return USP_ERR_INVALID_ARG;
+  long long row = (long long)H * D * elem_bytes;
+  int div = cp_size * ulysses_degree * (layout == USP_LAYOUT_ZIGZAG ? 2 : 1);
+  if (S % div != 0) return USP_ERR_INVALID_ARG;
+  if ((double)B * S * row / 16.0 >= 2147483647.0) return USP_ERR_UNSUPPORTED;
+  if (B * (long long)S > 0 && (!src || !dst)) return USP_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return USP_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  switch (kind) {
+    case USP_PERMUTE_EXTRACT:
+    case USP_PERMUTE_RESTORE:
+      if (row % 16 != 0) return USP_ERR_INVALID_ARG;
+      return launch_permute_layout(src, dst, B, S, (int)row, layout, cp_size,
+                                   kind == USP_PERMUTE_RESTORE, st);
+    case USP_PERMUTE_ULYSSES_SEQ2HEAD:
+    case USP_PERMUTE_ULYSSES_HEAD2SEQ:
+      if (H % ulysses_degree != 0 || (row / ulysses_degree) % 16 != 0)
+        return USP_ERR_INVALID_ARG;
+      return launch_ulysses(src, dst, B, S, (int)row, ulysses_degree,
+                            kind == USP_PERMUTE_ULYSSES_SEQ2HEAD, st);
+  }
+  return USP_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

@@ -1,0 +1,526 @@
+// Ring attention forward on the 5th-generation tensor cores (tcgen05), bf16
+// inputs with fp32 accumulation in tensor memory.
+//
+// What it computes is the per-rank ring schedule of "Long Context
+// Attention" ("Ring Attention": KV shards travel the ring until every host
+// has seen all of them; "Tree Attention": partials merge with the
+// associative log-sum-exp rule): for virtual ring rank rho the KV shards are
+// visited in the order kappa = rho, rho-1, ..., and every visited key tile
+// is folded into the running partial (row max m, row sum l, O accumulator),
+// which is the unnormalised form of a merged (O, LSE) partial.
+//
+// One CTA owns two 128-row query tiles of one (batch, head) of the same
+// ring rank. Roles (320 threads):
+//   warps 0-3   softmax group 0: one query row of tile 0 per thread
+//   warps 4-7   softmax group 1: one query row of tile 1 per thread
+//   warp  8     producer: classifies key tiles (empty / full / masked) and
+//               streams K and V tiles with TMA into two-slot rings
+//   warp  9     MMA issuer (one thread) and owner of the tensor memory
+// Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128),
+// overwritten in place by P_i (bf16 pairs, first 64 columns) which feeds
+// O_i += P_i V as the A operand from tensor memory; O_i at 256 + D i.
+// The two tiles ping-pong: while one group turns S into P, the tensor core
+// runs the other tile's P V and next Q K^T.
+// Masks are resolved per 128x128 tile: empty tiles are never loaded, full
+// tiles run without any mask arithmetic, masked tiles test each element
+// against the row's visible interval. The running max is only moved (and O
+// rescaled) when it grows by more than 2^8, which keeps the result exact
+// while skipping most rescales.
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace usp {
+namespace {
+
+using namespace tc;
+
+// Device status word of this kernel family (USP_ERR_TIMEOUT after a wait
+// gave up); read and cleared by usp_device_status().
+__device__ int g_fwd_tc_status = 0;
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per tile
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEmpty = 0, kFull = 1, kMasked = 2;
+constexpr int kEnd = -1;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct Smem {
+  static constexpr int kHalves = D / 64;              // 128-byte swizzle rows
+  static constexpr int kTileBytes = kBM * D * 2;       // one 128 x D bf16 tile
+  static constexpr int kHalfBytes = kBM * 128;         // 128 rows x 128 bytes
+  // offsets from the 1024-aligned base
+  static constexpr int kQ = 0;                          // 2 query tiles
+  static constexpr int kK = kQ + 2 * kTileBytes;        // 2 key slots
+  static constexpr int kV = kK + 2 * kTileBytes;        // 2 value slots
+  static constexpr int kBar = kV + 2 * kTileBytes;
+  // barriers (8 bytes each)
+  static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5,
+                       kVEmpty = 7, kSFull = 9, kPFull = 11, kOFull = 13,
+                       kInfoFull = 15, kMmaDone = 17, kNumBars = 18;
+  static constexpr int kSched = kBar + 8 * kNumBars;    // int4 x 2
+  static constexpr int kInfo = kSched + 32;             // int2 x 2
+  static constexpr int kMisc = kInfo + 16;              // tmem base, abort
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;          // alignment slack
+};
+
+struct TileSpan {
+  int lo, hi, step;  // natural positions lo, lo+step, ..., hi
+};
+
+__device__ __forceinline__ TileSpan tile_span(const AttnParams& P, int base) {
+  TileSpan t;
+  t.lo = nat_pos(P, base);
+  t.step = (P.layout == kStripe) ? P.cp : 1;
+  t.hi = t.lo + (kBM - 1) * t.step;
+  return t;
+}
+
+// empty / full / masked for one query tile against one key tile. Positions
+// inside each tile are increasing (tiles never cross a chunk), so the tile
+// extremes decide.
+__device__ int classify(const AttnParams& P, const TileSpan& q, const TileSpan& k) {
+  int qlo = q.lo, qhi = q.hi, klo = k.lo, khi = k.hi;
+  if (P.cu != nullptr) {
+    int sq0 = seg_of(P.cu, P.nseq, qlo), sq1 = seg_of(P.cu, P.nseq, qhi);
+    int sk0 = seg_of(P.cu, P.nseq, klo), sk1 = seg_of(P.cu, P.nseq, khi);
+    if (sk1 < sq0 || sk0 > sq1) return kEmpty;
+    if (!(sq0 == sq1 && sk0 == sk1 && sq0 == sk0)) return kMasked;
+    int st = __ldg(P.cu + sq0);
+    qlo -= st; qhi -= st; klo -= st; khi -= st;
+  }
+  if (P.causal && klo > qhi) return kEmpty;
+  bool full = !P.causal || khi <= qlo;
+  if (P.window > 0) {
+    bool any_window = qlo - khi < P.window || !P.causal && khi > qlo;
+    bool any_sink = klo < P.sink;
+    if (!any_window && !any_sink) return kEmpty;
+    bool all_window = qhi - klo < P.window || khi < P.sink;
+    full = full && all_window;
+  }
+  return full ? kFull : kMasked;
+}
+
+// Heavy-first ordering of query-tile pairs (so the hardware block scheduler
+// approximates longest-processing-time-first): causal dense problems visit
+// pairs by decreasing natural position.
+__device__ __forceinline__ int pair_for_rank(const AttnParams& P, int r, int npairs) {
+  if (!P.causal || P.cu != nullptr) return r;
+  if (P.layout == kStripe) {
+    int ppr = P.shard / (2 * kBM);
+    int t_local = ppr - 1 - r / P.cp;
+    int rho = r % P.cp;
+    return rho * ppr + t_local;
+  }
+  int pos = (npairs - 1 - r) * (2 * kBM);
+  if (P.layout == kContiguous) return pos / (2 * kBM);
+  int C = P.chunk, c = pos / C, off = pos - c * C, rho, p;
+  if (c < P.cp) {
+    rho = c;
+    p = rho * P.shard + off;
+  } else {
+    rho = 2 * P.cp - 1 - c;
+    p = rho * P.shard + C + off;
+  }
+  return p / (2 * kBM);
+}
+
+template <int D>
+// 320 threads x 200 registers fit the SM's 64K register file.
+__global__ void __maxnreg__(200)
+attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
+  int4* sched = reinterpret_cast<int4*>(sm + L::kSched);
+  int2* info = reinterpret_cast<int2*>(sm + L::kInfo);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int npairs = P.S / (2 * kBM);
+  const int hb = blockIdx.x % (P.Hq * P.Bt);
+  const int pair = pair_for_rank(P, blockIdx.x / (P.Hq * P.Bt), npairs);
+  const int h = hb / P.Bt, bt = hb % P.Bt;
+  const int g = h / P.G;
+  const int qbase0 = pair * 2 * kBM;          // permuted row of tile 0
+  const int rho = qbase0 / P.shard;           // ring rank of both tiles
+  const int tiles_per_shard = P.shard / kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kQFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+      mbar_init(bar(L::kSFull + s), 1);
+      mbar_init(bar(L::kPFull + s), kBM);
+      mbar_init(bar(L::kOFull + s), 1);
+      mbar_init(bar(L::kInfoFull + s), 1);
+    }
+    mbar_init(bar(L::kMmaDone), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(sbase + L::kMisc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch(&tm_q);
+      tma_prefetch(&tm_k);
+      tma_prefetch(&tm_v);
+      const TileSpan q0 = tile_span(P, qbase0), q1 = tile_span(P, qbase0 + kBM);
+      mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
+      for (int i = 0; i < 2; ++i)
+        for (int hf = 0; hf < L::kHalves; ++hf)
+          tma_load_4d(sbase + L::kQ + i * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
+                      bar(L::kQFull), hf * 64, h, qbase0 + i * kBM, bt);
+      int n = 0;
+      bool ok = true;
+      for (int s = 0; s < P.cp && ok; ++s) {
+        const int kap = (rho - s + P.cp) % P.cp;
+        for (int t = 0; t < tiles_per_shard && ok; ++t) {
+          const int kt = kap * tiles_per_shard + t;
+          const TileSpan ks = tile_span(P, kt * kBN);
+          const int c0 = classify(P, q0, ks), c1 = classify(P, q1, ks);
+          if (c0 == kEmpty && c1 == kEmpty) continue;
+          const int slot = n & 1, use = n >> 1;
+          if (use >= 1 && !(ok = mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1,
+                                           abort_flag, P.status)))
+            break;
+          sched[slot] = make_int4(kt, c0, c1, 0);
+          mbar_expect_tx(bar(L::kKFull + slot), L::kTileBytes);
+          for (int hf = 0; hf < L::kHalves; ++hf)
+            tma_load_4d(sbase + L::kK + slot * L::kTileBytes + hf * L::kHalfBytes,
+                        &tm_k, bar(L::kKFull + slot), hf * 64, g, kt * kBN, bt);
+          if (use >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + slot), (use - 1) & 1,
+                                           abort_flag, P.status)))
+            break;
+          mbar_expect_tx(bar(L::kVFull + slot), L::kTileBytes);
+          for (int hf = 0; hf < L::kHalves; ++hf)
+            tma_load_4d(sbase + L::kV + slot * L::kTileBytes + hf * L::kHalfBytes,
+                        &tm_v, bar(L::kVFull + slot), hf * 64, g, kt * kBN, bt);
+          ++n;
+        }
+      }
+      if (ok) {
+        const int slot = n & 1, use = n >> 1;
+        if (use < 1 || mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1, abort_flag,
+                                 P.status)) {
+          sched[slot] = make_int4(kEnd, 0, 0, 0);
+          mbar_arrive(bar(L::kKFull + slot));
+        }
+        // tail: every issued copy has been consumed before the CTA may exit
+        for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m) {
+          const int sl = m & 1, us = m >> 1;
+          if (!mbar_wait(bar(L::kVEmpty + sl), us & 1, abort_flag, P.status)) break;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    // Issue order per key tile n (e0/e1: tile n is non-empty for query tile
+    // 0/1): QK0(n), PV1(previous tile of query tile 1), release V slot of
+    // tile n-1, QK1(n), release K slot of n, PV0(n). QK_i(n) is always issued
+    // after PV_i of i's previous tile, so S_i may overwrite P_i in place.
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = idesc_bf16_f32(kBM, kBN, 0, 0);
+      constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, 0, 1);
+      const uint32_t s_tm[2] = {tmem, tmem + 128};
+      const uint32_t o_tm[2] = {tmem + 256, tmem + 256 + D};
+      int cnt[2] = {0, 0};  // QK issued per query tile
+      bool ok = mbar_wait(bar(L::kQFull), 0, abort_flag, P.status);
+      auto qk = [&](int i, int slot) {
+        const uint32_t qa = sbase + L::kQ + i * L::kTileBytes;
+        const uint32_t ka = sbase + L::kK + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          mma_ss(s_tm[i], sdesc_sw128(qa + off, 16, 1024),
+                 sdesc_sw128(ka + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kSFull + i));
+        ++cnt[i];
+      };
+      // O_i (+)= P_i V(slot); waits for P_i of the latest QK_i and for V.
+      auto pv = [&](int i, int slot, int use, int first) -> bool {
+        if (!mbar_wait(bar(L::kPFull + i), (cnt[i] - 1) & 1, abort_flag, P.status))
+          return false;
+        if (!mbar_wait(bar(L::kVFull + slot), use & 1, abort_flag, P.status))
+          return false;
+        tc_fence_after();
+        const uint32_t va = sbase + L::kV + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(o_tm[i], s_tm[i] + kk * 8,
+                 sdesc_sw128(va + kk * 2048, L::kHalfBytes, 1024), kIdPV,
+                 (first && kk == 0) ? 0u : 1u);
+        return true;
+      };
+      int n = 0;
+      int first[2] = {1, 1};
+      int pend_slot = -1, pend_use = 0, pend_first = 0;  // PV1 still to issue
+      int prev_slot = -1;                                // V slot of tile n-1
+      while (ok) {
+        const int slot = n & 1, use = n >> 1;
+        if (!(ok = mbar_wait(bar(L::kKFull + slot), use & 1, abort_flag, P.status)))
+          break;
+        const int4 e = sched[slot];
+        if (e.x == kEnd) break;
+        tc_fence_after();
+        const bool e0 = e.y != kEmpty, e1 = e.z != kEmpty;
+        if (e0) {
+          info[0] = make_int2(e.x, e.y);
+          mbar_arrive(bar(L::kInfoFull + 0));
+          qk(0, slot);
+        }
+        if (pend_slot >= 0) {
+          if (!(ok = pv(1, pend_slot, pend_use, pend_first))) break;
+          pend_slot = -1;
+        }
+        if (prev_slot >= 0) mma_commit(bar(L::kVEmpty + prev_slot));
+        if (e1) {
+          info[1] = make_int2(e.x, e.z);
+          mbar_arrive(bar(L::kInfoFull + 1));
+          qk(1, slot);
+        }
+        mma_commit(bar(L::kKEmpty + slot));
+        if (e0) {
+          if (!(ok = pv(0, slot, use, first[0]))) break;
+          first[0] = 0;
+        }
+        if (e1) {
+          pend_slot = slot;
+          pend_use = use;
+          pend_first = first[1];
+          first[1] = 0;
+        }
+        prev_slot = slot;
+        ++n;
+      }
+      if (ok && pend_slot >= 0) ok = pv(1, pend_slot, pend_use, pend_first);
+      if (ok && prev_slot >= 0) mma_commit(bar(L::kVEmpty + prev_slot));
+      for (int i = 0; i < 2; ++i) {
+        mma_commit(bar(L::kOFull + i));
+        info[i] = make_int2(kEnd, 0);
+        mbar_arrive(bar(L::kInfoFull + i));
+      }
+      // nothing of ours may still run on the tensor core when TMEM is freed
+      mma_commit(bar(L::kMmaDone));
+      mbar_wait(bar(L::kMmaDone), 0, abort_flag, P.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int i = warp >> 2;                 // query tile of this group
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;       // row within the tile = TMEM lane
+    const int prow = qbase0 + i * kBM + r;   // permuted query row
+    const RowMask rm = row_mask(P, nat_pos(P, prow));
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + 128 * i;
+    const uint32_t o_tm = tmem + lane_off + 256 + D * i;
+    float m_run = -INFINITY, l_run = 0.f;
+    int c = 0;
+    bool ok = true;
+    while (true) {
+      ok = mbar_wait(bar(L::kInfoFull + i), c & 1, abort_flag, P.status);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      const int2 inf = info[i];
+      if (inf.x == kEnd) break;
+      ok = mbar_wait(bar(L::kSFull + i), c & 1, abort_flag, P.status);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tm + 32 * ch, sr[ch]);
+      tmem_wait_ld();
+      if (inf.y == kMasked) {
+        const TileSpan ks = tile_span(P, inf.x * kBN);
+#pragma unroll
+        for (int j = 0; j < 128; ++j)
+          if (!row_visible(rm, ks.lo + j * ks.step))
+            sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
+      }
+      float mx = __uint_as_float(sr[0][0]);
+#pragma unroll
+      for (int j = 1; j < 128; ++j) mx = fmaxf(mx, __uint_as_float(sr[j >> 5][j & 31]));
+      mx *= P.scale_log2;
+      // lazy rescale: move the running max only when it grows by > 2^8
+      const bool need = mx > m_run + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx);
+        m_run = mx;
+      }
+      l_run *= alpha;
+      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+      float lsum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int j0 = 64 * ch + 2 * j;
+          const float p0 = ex2(fmaf(__uint_as_float(sr[j0 >> 5][j0 & 31]), P.scale_log2, -msub));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[(j0 + 1) >> 5][(j0 + 1) & 31]),
+                                    P.scale_log2, -msub));
+          lsum += p0 + p1;
+          pk[j] = pack_bf16(p0, p1);
+        }
+        tmem_st32(s_tm + 32 * ch, pk);
+      }
+      l_run += lsum;
+      // O_i holds PV of the previous tiles (complete: the commit that
+      // signalled S_i tracks every earlier MMA); rescale it to the new max
+      // before P_i V is accumulated onto it.
+      if (__any_sync(0xffffffffu, need && c > 0)) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(o_tm + 32 * ch, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(o_tm + 32 * ch, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::kPFull + i));
+      ++c;
+    }
+    // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2
+    if (ok) ok = mbar_wait(bar(L::kOFull + i), 0, abort_flag, P.status);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(P.o) +
+                          (((long long)bt * P.S + prow) * P.Hq + h) * D;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t o[32];
+      tmem_ld32(o_tm + 32 * ch, o);
+      tmem_wait_ld();
+      uint4 w[4];
+      uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float a = (c > 0) ? __uint_as_float(o[2 * j]) * inv : 0.f;
+        const float b = (c > 0) ? __uint_as_float(o[2 * j + 1]) * inv : 0.f;
+        wp[j] = pack_bf16(a, b);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dst[j] = w[j];
+    }
+    P.lse[lse_index(P, bt, h, prow)] =
+        (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [Bt][S][H][D] bf16 -> 4-D map (D, H, S, Bt), box (64, 1, 128, 1), 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)Bt};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                           (cuuint64_t)S * H * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kBM, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
+      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D))
+    return USP_ERR_CUDA;
+  const int smem = Smem<D>::kAlloc;
+  static int* status = nullptr;
+  if (status == nullptr &&
+      cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_fwd_tc_status) != cudaSuccess)
+    return USP_ERR_CUDA;
+  AttnParams Pk = P;
+  Pk.status = status;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return USP_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long blocks = (long long)(P.S / (2 * kBM)) * P.Hq * P.Bt;
+  {
+    ProfScope ps(st, "attn_fwd_tc");
+    attn_fwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv);
+  }
+  note_launch();
+  return check_launch();
+}
+
+}  // namespace
+
+int read_clear_fwd_tc_status() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fwd_tc_status, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) cudaMemcpyToSymbol(g_fwd_tc_status, &z, sizeof(int));
+  return v;
+}
+
+bool fwd_tc_supported(const AttnParams& P) {
+  if (P.D != 128 && P.D != 64) return false;
+  if (P.shard % (2 * kBM) != 0) return false;
+  if (P.layout == kZigzag && P.chunk % (2 * kBM) != 0) return false;
+  return true;
+}
+
+usp_status_t launch_fwd_tc(const AttnParams& P, cudaStream_t st) {
+  return P.D == 128 ? launch_d<128>(P, st) : launch_d<64>(P, st);
+}
+
+}  // namespace usp

@@ -1,0 +1,56 @@
+// Host-side declarations shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "../../include/usp.h"
+#include "common.cuh"
+
+namespace usp {
+
+// Counts kernel launches enqueued by this library (usp_launch_count()).
+void note_launch(int n = 1);
+
+// Converts the last CUDA error (after a launch) into a status.
+usp_status_t check_launch();
+
+// Brackets one kernel launch with timing events when the kernel timer is on
+// (usp_profile_enable); a no-op otherwise.
+struct ProfScope {
+  int idx;
+  cudaStream_t st;
+  ProfScope(cudaStream_t s, const char* name);
+  ~ProfScope();
+};
+
+// permute.cu
+usp_status_t launch_permute_layout(const void* src, void* dst, int B, int S,
+                                   int row_bytes, int layout, int cp,
+                                   int restore, cudaStream_t st);
+usp_status_t launch_ulysses(const void* src, void* dst, int B, int S,
+                            int row_bytes, int ud, int seq2head,
+                            cudaStream_t st);
+
+// merge.cu
+usp_status_t launch_merge(const float* o_parts, const float* lse_parts, int n,
+                          long long rows, int D, int tree, void* o_out,
+                          int out_bf16, float* lse_out, cudaStream_t st);
+
+// attn_simt.cu (CUDA-core kernels, fp32 arithmetic; any supported shape)
+usp_status_t launch_fwd_simt(const AttnParams& P, int bf16, cudaStream_t st);
+usp_status_t launch_bwd_preprocess(const AttnParams& P, int bf16,
+                                   int zero_dq_acc, cudaStream_t st);
+usp_status_t launch_bwd_simt(const AttnParams& P, int bf16, cudaStream_t st);
+
+// attn_fwd_tc.cu (tcgen05 tensor-core forward, bf16)
+bool fwd_tc_supported(const AttnParams& P);
+usp_status_t launch_fwd_tc(const AttnParams& P, cudaStream_t st);
+
+int read_clear_fwd_tc_status();  // -1 on a CUDA error
+
+// attn_bwd_tc.cu (tcgen05 tensor-core backward, bf16)
+bool bwd_tc_supported(const AttnParams& P);
+usp_status_t launch_bwd_tc(const AttnParams& P, cudaStream_t st);
+int read_clear_bwd_tc_status();  // -1 on a CUDA error
+
+}  // namespace usp

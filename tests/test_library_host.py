@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol include/usp.h declares, and rejects invalid arguments before any
+launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import sequence_long_context_gb300 as usp
+from sequence_long_context_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "usp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(usp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(_lib.SIGNATURES) == names
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["USP_OK", "USP_ERR_INVALID_ARG", "USP_ERR_UNSUPPORTED",
+                                 "USP_ERR_ALIGNMENT", "USP_ERR_WORKSPACE", "USP_ERR_CUDA",
+                                 "USP_ERR_TIMEOUT"]):
+        assert lib.usp_status_string(code).decode() == name
+
+
+def test_workspace_sizes(lib):
+    # ud=1 forward needs no scratch; ud=2 holds q,k,v,o in head-grouped form
+    assert usp.usp_attn_fwd_workspace_size(2, 8192, 32, 32, 128, 4, 1, 0) == 0
+    n = usp.usp_attn_fwd_workspace_size(2, 8192, 32, 32, 128, 4, 2, 0)
+    assert n == 4 * 2 * 8192 * 32 * 128 * 2
+    b = usp.usp_attn_bwd_workspace_size(1, 1024, 8, 2, 64, 2, 1, 1)
+    assert b >= 8 * 1024 * 4
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced
+
+
+def fwd(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, B=1, S=256, Hq=4, Hkv=2,
+             D=64, scale=0.0, causal=1, window=0, sink=0, cu=None, cp=4, ud=1,
+             layout=1, dtype=1, flags=0, ws=None, wsb=0, stream=None)
+    a.update(over)
+    return lib.usp_attn_fwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["S"],
+                            a["Hq"], a["Hkv"], a["D"], a["scale"], a["causal"],
+                            a["window"], a["sink"], a["cu"], a["cp"], a["ud"],
+                            a["layout"], a["dtype"], a["flags"], a["ws"], a["wsb"],
+                            a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Hq=3), 1),               # Hq % Hkv
+    (dict(S=250), 1),              # zigzag needs S % (2 cp) == 0
+    (dict(layout=0, S=254), 1),    # contiguous needs S % cp == 0
+    (dict(D=96), 2),               # head dim not supported
+    (dict(cp=0), 1),
+    (dict(ud=4), 1),               # Hkv=2 not divisible by ud=4
+    (dict(layout=7), 1),
+    (dict(sink=-1), 1),
+    (dict(q=FAKE + 8), 3),         # misaligned
+    (dict(q=None), 1),             # null tensor
+    (dict(ud=2), 4),               # Ulysses needs workspace
+])
+def test_fwd_rejects_before_launch(lib, over, code):
+    assert fwd(lib, **over) == code
+
+
+def test_permute_and_merge_reject(lib):
+    # elem_bytes, layout, divisibility, alignment
+    assert lib.usp_permute(FAKE, FAKE, 0, 1, 1, 100, 2, 64, 4, 1, 3, None) == 1
+    assert lib.usp_permute(FAKE, FAKE, 0, 9, 1, 128, 2, 64, 4, 1, 2, None) == 1
+    assert lib.usp_permute(FAKE, FAKE, 0, 1, 1, 100, 2, 64, 4, 1, 2, None) == 1
+    assert lib.usp_permute(FAKE + 4, FAKE, 0, 1, 1, 128, 2, 64, 4, 1, 2, None) == 3
+    assert lib.usp_permute(FAKE, FAKE, 2, 1, 1, 128, 3, 64, 4, 2, 2, None) == 1
+    assert lib.usp_merge_partials(FAKE, FAKE, 0, 10, 128, 0, FAKE, 1, FAKE, None) == 1
+    assert lib.usp_merge_partials(FAKE, FAKE, 65, 10, 128, 1, FAKE, 1, FAKE, None) == 1
+    assert lib.usp_merge_partials(FAKE, FAKE, 2, 10, 96, 0, FAKE, 1, FAKE, None) == 1
+    assert lib.usp_merge_partials(FAKE, FAKE + 4, 2, 10, 128, 0, FAKE, 1, FAKE, None) == 3
+
+
+def test_empty_problem_is_a_no_op(lib):
+    # S == 0 validates and returns OK without touching the device
+    assert fwd(lib, S=0, q=None, k=None, v=None, out=None, lse=None) == 0
+
+
+def test_python_binding_raises(lib):
+    with pytest.raises(usp.UspError, match="USP_ERR_INVALID_ARG"):
+        usp._check(1)

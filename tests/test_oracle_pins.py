@@ -369,3 +369,22 @@ def test_pin_catches_planted_mistakes(monkeypatch):
     monkeypatch.setattr(attention, "visibility", off_by_one)
     O, _ = attention.attn_fwd(q, k, v, 0.3, True, 5, 0)
     assert np.abs(O - o_ref.numpy()).max() > 1e-3
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_sampled_bwd_matches_full(varlen):
+    S, Hq, Hkv, D = 40, 6, 2, 8
+    cu = [0, 13, 14, 40] if varlen else None
+    if varlen:
+        q, k, v, do = rnd((S, Hq, D), 70), rnd((S, Hkv, D), 71), rnd((S, Hkv, D), 72), rnd((S, Hq, D), 73)
+    else:
+        q, k, v, do = rnd((2, S, Hq, D), 70), rnd((2, S, Hkv, D), 71), rnd((2, S, Hkv, D), 72), rnd((2, S, Hq, D), 73)
+    kw = dict(causal=True, window=9, sink_tokens=2, cu_seqlens=cu)
+    dq, dk, dv = attention.attn_bwd(q, k, v, do, 0.4, **kw)
+    b = 0 if varlen else 1
+    rows, keys = [0, 5, 13, 14, 39], [0, 1, 12, 20, 39]
+    sq, sk, sv = attention.attn_bwd_sampled(q, k, v, do, 0.4, b, 1, rows, keys, **kw)
+    sel = (lambda t: t) if varlen else (lambda t: t[b])
+    np.testing.assert_allclose(sq, np.transpose(sel(dq)[rows][:, 3:6], (1, 0, 2)), atol=1e-12)
+    np.testing.assert_allclose(sk, sel(dk)[keys, 1], atol=1e-12)
+    np.testing.assert_allclose(sv, sel(dv)[keys, 1], atol=1e-12)
