@@ -250,6 +250,10 @@ int usp_profile_read(usp_kernel_stat_t *stats, int max_stats);
  * Synchronises the whole device: a diagnostics call, not for hot loops. */
 usp_status_t usp_device_status(void);
 
+/* Which CUDA call failed, and why, for the last USP_ERR_CUDA returned on the
+ * calling thread (thread-local storage, never NULL; empty if none). */
+const char *usp_last_error_detail(void);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *usp_status_string(usp_status_t status);
 

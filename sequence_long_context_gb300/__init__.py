@@ -45,7 +45,10 @@ def _stream(stream) -> Optional[int]:
 
 def _check(status: int) -> None:
     if status != 0:
-        name = _lib.load().usp_status_string(status).decode()
+        lib = _lib.load()
+        name = lib.usp_status_string(status).decode()
+        if name == "USP_ERR_CUDA":
+            name += ": " + lib.usp_last_error_detail().decode()
         raise UspError(name)
 
 

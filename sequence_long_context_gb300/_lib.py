@@ -26,6 +26,7 @@ SIGNATURES = {
     "usp_profile_enable": (_i, [_i]),
     "usp_profile_read": (_i, [_vp, _i]),
     "usp_device_status": (_i, []),
+    "usp_last_error_detail": (_c.c_char_p, []),
 }
 
 

@@ -5,6 +5,7 @@
 // scratch is carved out of the caller's workspace in 256-byte aligned slices.
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <map>
 #include <string>
@@ -52,9 +53,20 @@ ProfScope::~ProfScope() {
 
 void note_launch(int n) { g_launches.fetch_add((unsigned long long)n); }
 
+static thread_local char g_detail[256] = "";
+
+usp_status_t fail_cuda_msg(const char* where, const char* msg) {
+  std::snprintf(g_detail, sizeof(g_detail), "%s: %s", where, msg);
+  return USP_ERR_CUDA;
+}
+
+usp_status_t fail_cuda(const char* where, cudaError_t e) {
+  return fail_cuda_msg(where, cudaGetErrorString(e));
+}
+
 usp_status_t check_launch() {
   cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? USP_OK : USP_ERR_CUDA;
+  return e == cudaSuccess ? USP_OK : fail_cuda("kernel launch", e);
 }
 
 namespace {
@@ -217,6 +229,8 @@ const char* usp_status_string(usp_status_t st) {
 }
 
 uint64_t usp_launch_count(void) { return g_launches.load(); }
+
+const char* usp_last_error_detail(void) { return g_detail; }
 
 usp_status_t usp_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return USP_ERR_CUDA;

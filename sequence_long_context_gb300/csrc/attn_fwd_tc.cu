@@ -28,6 +28,8 @@
 // while skipping most rescales.
 #include <cudaTypedefs.h>
 
+#include <cstdio>
+
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -133,8 +135,8 @@ __device__ __forceinline__ int pair_for_rank(const AttnParams& P, int r, int npa
 }
 
 template <int D>
-// 320 threads x 200 registers fit the SM's 64K register file.
-__global__ void __maxnreg__(200)
+// 10 warps: three share a 16K-register sub-partition, so <= 168 each.
+__global__ void __maxnreg__(168)
 attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v) {
@@ -461,7 +463,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [Bt][S][H][D] bf16 -> 4-D map (D, H, S, Bt), box (64, 1, 128, 1), 128B swizzle.
 bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn) {
+    fail_cuda_msg("cuTensorMapEncodeTiled", "driver entry point not found");
+    return false;
+  }
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)Bt};
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
                            (cuuint64_t)S * H * D * 2};
@@ -471,7 +476,13 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    std::snprintf(msg, sizeof(msg), "CUresult %d", (int)r);
+    fail_cuda_msg("cuTensorMapEncodeTiled", msg);
+    return false;
+  }
+  return true;
 }
 
 template <int D>
@@ -479,19 +490,20 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
       !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D))
-    return USP_ERR_CUDA;
+    return USP_ERR_CUDA;  // detail recorded by make_map
   const int smem = Smem<D>::kAlloc;
   static int* status = nullptr;
-  if (status == nullptr &&
-      cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_fwd_tc_status) != cudaSuccess)
-    return USP_ERR_CUDA;
+  if (status == nullptr) {
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_fwd_tc_status);
+    if (e != cudaSuccess) return fail_cuda("cudaGetSymbolAddress(status)", e);
+  }
   AttnParams Pk = P;
   Pk.status = status;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return USP_ERR_CUDA;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(smem)", e);
     attr_set = true;
   }
   const long long blocks = (long long)(P.S / (2 * kBM)) * P.Hq * P.Bt;

@@ -14,6 +14,11 @@ void note_launch(int n = 1);
 // Converts the last CUDA error (after a launch) into a status.
 usp_status_t check_launch();
 
+// Records a human-readable reason for the USP_ERR_CUDA about to be returned
+// (usp_last_error_detail()); returns USP_ERR_CUDA.
+usp_status_t fail_cuda(const char* where, cudaError_t e);
+usp_status_t fail_cuda_msg(const char* where, const char* msg);
+
 // Brackets one kernel launch with timing events when the kernel timer is on
 // (usp_profile_enable); a no-op otherwise.
 struct ProfScope {
