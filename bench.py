@@ -316,7 +316,9 @@ def main():
                          "share": tot / max(1e-9, sum(t for _, t in kstats.values()))}
     # dominant kernel and its algorithmic work per launch
     fwd_k = [k for k in kernels if k.startswith("attn_fwd")]
-    bwd_k = [k for k in kernels if k.startswith("attn_bwd") and "preprocess" not in k]
+    # the backward's contraction kernels (not its HBM-bound preprocess/convert)
+    bwd_k = [k for k in kernels if k.startswith("attn_bwd")
+             and "preprocess" not in k and "convert" not in k]
     cand = []
     for k in fwd_k:
         cand.append((kstats[k][1], k, F["fwd"]))

@@ -166,13 +166,17 @@ FwdWs carve_fwd(Carve& c, const Shape& s) {
 
 struct BwdWs {
   float* delta;
+  float* lse2;
   float* dq_acc;
   void *q, *k, *v, *o, *dout, *dq, *dk, *dv;
 };
 BwdWs carve_bwd(Carve& c, const Shape& s, bool tc) {
   BwdWs w{};
   w.delta = static_cast<float*>(c.take((size_t)s.B_eff() * s.Hq * s.S * 4));
-  if (tc) w.dq_acc = static_cast<float*>(c.take((size_t)s.B_eff() * s.S * s.Hq * s.D * 4));
+  if (tc) {
+    w.lse2 = static_cast<float*>(c.take((size_t)s.B_eff() * s.Hq * s.S * 4));
+    w.dq_acc = static_cast<float*>(c.take((size_t)s.B_eff() * s.S * s.Hq * s.D * 4));
+  }
   if (s.ud > 1) {
     w.q = c.take(s.q_bytes());
     w.k = c.take(s.kv_bytes());
@@ -374,6 +378,7 @@ usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
   }
   P.lse = const_cast<float*>(lse);
   P.delta = w.delta;
+  P.lse2 = w.lse2;
   P.dq_acc = w.dq_acc;
   if ((r = launch_bwd_preprocess(P, dtype == USP_BF16, tc ? 1 : 0, st)) != USP_OK)
     return r;

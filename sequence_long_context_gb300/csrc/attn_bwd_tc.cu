@@ -1,8 +1,553 @@
-// tcgen05 tensor-core backward (bf16 in, fp32 accumulate). Not yet enabled.
+// Ring attention backward on the tcgen05 tensor cores (bf16 in, fp32 acc).
+//
+// Gradient of the ring forward from its saved LSE ("Long Context Attention"
+// notes, "Motivation": QKV, output, LSE and dout are what the backward
+// needs). With P = exp(scale q.k - LSE) and Delta_i = <dO_i, O_i>:
+//   dV = P^T dO,  dS = P * (dO V^T - Delta),  dK = scale dS^T Q,
+//   dQ = scale dS K.
+// One CTA owns one 128-key tile of one KV head. The shard the tile belongs
+// to visits the query ranks in ring order (kappa, kappa+1, ...), and for each
+// query tile every query head of the GQA group is taken in turn, so dK and
+// dV accumulate in tensor memory over the whole ring and the group and are
+// written once (the shard's ring return). dQ contributions are added into an
+// fp32 accumulator in global memory with vector reductions.
+//
+// Roles (320 threads):
+//   warps 0-3  softmax group, one key row per thread: P^T = exp2(S^T - LSE),
+//              dS^T = P^T (dP^T - Delta); P^T and dS^T go back to tensor
+//              memory as bf16 (A operands of dV and dK) and dS to shared
+//              memory (A operand of dQ)
+//   warps 4-7  dQ group, one query row per thread: drains the dQ tile from
+//              tensor memory into the global accumulator
+//   warp 8     producer: K, V once; then Q, dO tiles through a 2-slot ring
+//   warp 9     MMA issuer and tensor-memory owner
+// Tensor memory (512 columns): S^T [0,128) with P^T over its first 64 and
+// dQ[:, :64] over its last 64; dP^T [128,256) with dS^T over its first 64 and
+// dQ[:, 64:] over its last 64; dV [256, 256+D); dK [256+D, 256+2D).
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+
 #include "internal.h"
+#include "tc_ptx.cuh"
+#include "tile_sched.cuh"
 
 namespace usp {
-bool bwd_tc_supported(const AttnParams&) { return false; }
-usp_status_t launch_bwd_tc(const AttnParams&, cudaStream_t) { return USP_ERR_UNSUPPORTED; }
-int read_clear_bwd_tc_status() { return 0; }
+namespace {
+
+using namespace tc;
+
+__device__ int g_bwd_tc_status = 0;
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEnd = -1;
+
+template <int D>
+struct BSmem {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kHalfBytes = kTile * 128;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;        // 2 slots
+  static constexpr int kDO = kQ + 2 * kTileBytes;   // 2 slots
+  static constexpr int kDS = kDO + 2 * kTileBytes;  // 128 x 128 bf16
+  static constexpr int kBar = kDS + kTile * kTile * 2;
+  static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
+                       kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
+                       kDKVFull = 12, kMmaDone = 13, kNumBars = 14;
+  static constexpr int kSched = kBar + 8 * kNumBars;  // int4 x 2
+  static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
+  static constexpr int kMisc = kInfo + 32;            // tmem base, abort
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+// Visible query interval of one key (natural positions): a key at position j
+// of a sequence [s, e) is seen by queries i in [j (causal) or s,
+// j + window - 1 (window, unless j is one of the first sink_tokens) or e-1].
+struct ColMask {
+  int lo, hi;
+};
+
+__device__ __forceinline__ ColMask col_mask(const AttnParams& P, int j) {
+  int ks = 0, ke = P.S;
+  if (P.cu != nullptr) {
+    int n = seg_of(P.cu, P.nseq, j);
+    ks = __ldg(P.cu + n);
+    ke = __ldg(P.cu + n + 1);
+  }
+  ColMask m;
+  m.lo = P.causal ? j : ks;
+  m.hi = ke - 1;
+  if (P.window > 0 && j - ks >= P.sink) m.hi = min(m.hi, j + P.window - 1);
+  return m;
+}
+
+template <int D>
+__global__ void __maxnreg__(168)
+attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_do) {
+  using L = BSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
+  int4* sched = reinterpret_cast<int4*>(sm + L::kSched);
+  int4* info = reinterpret_cast<int4*>(sm + L::kInfo);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = P.S / kTile;
+  const int hb = blockIdx.x % (P.Hkv * P.Bt);
+  const int kt = ktile_for_rank(P, blockIdx.x / (P.Hkv * P.Bt), ntiles);
+  const int g = hb / P.Bt, bt = hb % P.Bt;
+  const int kappa = (kt * kTile) / P.shard;  // ring rank owning the key tile
+  const int tiles_per_shard = P.shard / kTile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kKVFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kQFull + s), 1);
+      mbar_init(bar(L::kQEmpty + s), 1);
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kDPFull), 1);
+    mbar_init(bar(L::kDSFull), kTile);
+    mbar_init(bar(L::kDQFull), 1);
+    mbar_init(bar(L::kDQEmpty), kTile);
+    mbar_init(bar(L::kInfoS), 1);
+    mbar_init(bar(L::kInfoQ), 1);
+    mbar_init(bar(L::kDKVFull), 1);
+    mbar_init(bar(L::kMmaDone), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(sbase + L::kMisc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch(&tm_q);
+      tma_prefetch(&tm_k);
+      tma_prefetch(&tm_v);
+      tma_prefetch(&tm_do);
+      const TileSpan ks = tile_span(P, kt * kTile);
+      mbar_expect_tx(bar(L::kKVFull), 2 * L::kTileBytes);
+      for (int hf = 0; hf < L::kHalves; ++hf) {
+        tma_load_4d(sbase + L::kK + hf * L::kHalfBytes, &tm_k, bar(L::kKVFull), hf * 64, g,
+                    kt * kTile, bt);
+        tma_load_4d(sbase + L::kV + hf * L::kHalfBytes, &tm_v, bar(L::kKVFull), hf * 64, g,
+                    kt * kTile, bt);
+      }
+      int n = 0;
+      bool ok = true;
+      // the key shard travels the ring: step s finds it on rank kappa + s
+      for (int s = 0; s < P.cp && ok; ++s) {
+        const int rho = (kappa + s) % P.cp;
+        for (int t = 0; t < tiles_per_shard && ok; ++t) {
+          const int qt = rho * tiles_per_shard + t;
+          const int cls = classify(P, tile_span(P, qt * kTile), ks);
+          if (cls == kClsEmpty) continue;
+          for (int hh = 0; hh < P.G && ok; ++hh) {
+            const int h = g * P.G + hh;
+            const int slot = n & 1, use = n >> 1;
+            if (use >= 1 && !(ok = mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1,
+                                             abort_flag, P.status)))
+              break;
+            sched[slot] = make_int4(qt, h, cls, 0);
+            mbar_expect_tx(bar(L::kQFull + slot), 2 * L::kTileBytes);
+            for (int hf = 0; hf < L::kHalves; ++hf) {
+              tma_load_4d(sbase + L::kQ + slot * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
+                          bar(L::kQFull + slot), hf * 64, h, qt * kTile, bt);
+              tma_load_4d(sbase + L::kDO + slot * L::kTileBytes + hf * L::kHalfBytes, &tm_do,
+                          bar(L::kQFull + slot), hf * 64, h, qt * kTile, bt);
+            }
+            ++n;
+          }
+        }
+      }
+      if (ok) {
+        const int slot = n & 1, use = n >> 1;
+        if (use < 1 || mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1, abort_flag,
+                                 P.status)) {
+          sched[slot] = make_int4(kEnd, 0, 0, 0);
+          mbar_arrive(bar(L::kQFull + slot));
+        }
+        for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
+          if (!mbar_wait(bar(L::kQEmpty + (m & 1)), (m >> 1) & 1, abort_flag, P.status))
+            break;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per query tile n: S^T = K Q^T, dP^T = V dO^T; after dS is ready:
+    // dQ = dS K (both D halves), then dV += P^T dO, dK += dS^T Q. The next
+    // S^T/dP^T overwrite the dQ columns, so they wait until dQ is drained.
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, 0, 0);
+      constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, 64, 1, 1);
+      constexpr uint32_t kIdKV = idesc_bf16_f32(kTile, D, 0, 1);
+      const uint32_t t_s = tmem, t_dp = tmem + 128;
+      const uint32_t t_dv = tmem + 256, t_dk = tmem + 256 + D;
+      const uint32_t ka = sbase + L::kK, va = sbase + L::kV, dsa = sbase + L::kDS;
+      bool ok = mbar_wait(bar(L::kKVFull), 0, abort_flag, P.status);
+      int n = 0;
+      while (ok) {
+        const int slot = n & 1, use = n >> 1;
+        if (!(ok = mbar_wait(bar(L::kQFull + slot), use & 1, abort_flag, P.status))) break;
+        const int4 e = sched[slot];
+        if (e.x == kEnd) break;
+        if (n > 0 && !(ok = mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status)))
+          break;
+        tc_fence_after();
+        info[0] = e;
+        mbar_arrive(bar(L::kInfoS));
+        info[1] = e;
+        mbar_arrive(bar(L::kInfoQ));
+        const uint32_t qa = sbase + L::kQ + slot * L::kTileBytes;
+        const uint32_t doa = sbase + L::kDO + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          mma_ss(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kSFull));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          mma_ss(t_dp, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
+                 kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kDPFull));
+        if (!(ok = mbar_wait(bar(L::kDSFull), n & 1, abort_flag, P.status))) break;
+        tc_fence_after();
+        // dQ[:, 64 hf : 64 hf + 64] = dS K[:, 64 hf : ...]  (K dim = keys)
+        for (int hf = 0; hf < L::kHalves; ++hf) {
+          const uint32_t dst = hf == 0 ? t_s + 64 : t_dp + 64;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(dst, sdesc_sw128(dsa + kk * 2048, L::kHalfBytes, 1024),
+                   sdesc_sw128(ka + hf * L::kHalfBytes + kk * 2048, L::kHalfBytes, 1024),
+                   kIdDQ, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kDQFull));
+        // dV += P^T dO ; dK += dS^T Q  (K dim = queries; A from tensor memory)
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(t_dv, t_s + kk * 8, sdesc_sw128(doa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(t_dk, t_dp + kk * 8, sdesc_sw128(qa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::kQEmpty + slot));
+        ++n;
+      }
+      mma_commit(bar(L::kDKVFull));
+      info[0] = make_int4(kEnd, n, 0, 0);
+      mbar_arrive(bar(L::kInfoS));
+      // the dQ group must have consumed the last real entry before the
+      // end marker overwrites it
+      if (ok && n > 0) mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status);
+      info[1] = make_int4(kEnd, n, 0, 0);
+      mbar_arrive(bar(L::kInfoQ));
+      mma_commit(bar(L::kMmaDone));
+      mbar_wait(bar(L::kMmaDone), 0, abort_flag, P.status);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int j = warp * 32 + lane;  // key row = TMEM lane
+    const int kp = kt * kTile + j;   // permuted key row
+    const ColMask cm = col_mask(P, nat_pos(P, kp));
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    uint8_t* ds_row = sm + L::kDS + j * 128;
+    int c = 0;
+    bool ok = true;
+    while (true) {
+      ok = mbar_wait(bar(L::kInfoS), c & 1, abort_flag, P.status);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      const int4 e = info[0];
+      if (e.x == kEnd) break;
+      const int qt = e.x, h = e.y;
+      const bool masked = e.z == kClsMasked;
+      const TileSpan qs = tile_span(P, qt * kTile);
+      const long long row_off = ((long long)bt * P.Hq + h) * P.S + (long long)qt * kTile;
+      const float* lse2 = P.lse2 + row_off;
+      const float* delta = P.delta + row_off;
+      ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      // P^T row (queries along columns) -> bf16 pairs into S^T columns [0, 64)
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32];
+        tmem_ld32(t_s + 32 * ch, sv);
+        float lv[32];
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(lse2 + 32 * ch) + k4);
+          lv[4 * k4] = x.x; lv[4 * k4 + 1] = x.y; lv[4 * k4 + 2] = x.z; lv[4 * k4 + 3] = x.w;
+        }
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float p0 = ex2(fmaf(__uint_as_float(sv[2 * k]), P.scale_log2, -lv[2 * k]));
+          float p1 = ex2(fmaf(__uint_as_float(sv[2 * k + 1]), P.scale_log2, -lv[2 * k + 1]));
+          if (masked) {
+            const int i0 = qs.lo + (32 * ch + 2 * k) * qs.step;
+            const int i1 = i0 + qs.step;
+            if (i0 < cm.lo || i0 > cm.hi) p0 = 0.f;
+            if (i1 < cm.lo || i1 > cm.hi) p1 = 0.f;
+          }
+          pk[k] = pack_bf16(p0, p1);
+        }
+        tmem_st16(t_s + 16 * ch, pk);
+      }
+      ok = mbar_wait(bar(L::kDPFull), c & 1, abort_flag, P.status);
+      // dS in shared memory is still read by the previous tile's dQ MMAs
+      if (ok && c > 0) ok = mbar_wait(bar(L::kDQFull), (c - 1) & 1, abort_flag, P.status);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      tmem_wait_st();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t dv[32], pv[16];
+        tmem_ld32(t_dp + 32 * ch, dv);
+        tmem_ld16(t_s + 16 * ch, pv);
+        float dl[32];
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(delta + 32 * ch) + k4);
+          dl[4 * k4] = x.x; dl[4 * k4 + 1] = x.y; dl[4 * k4 + 2] = x.z; dl[4 * k4 + 3] = x.w;
+        }
+        tmem_wait_ld();
+        uint32_t dk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          __nv_bfloat162 pp = *reinterpret_cast<__nv_bfloat162*>(&pv[k]);
+          const float2 pf = __bfloat1622float2(pp);
+          const float d0 = pf.x * (__uint_as_float(dv[2 * k]) - dl[2 * k]);
+          const float d1 = pf.y * (__uint_as_float(dv[2 * k + 1]) - dl[2 * k + 1]);
+          dk[k] = pack_bf16(d0, d1);
+        }
+        tmem_st16(t_dp + 16 * ch, dk);
+        // dS (queries contiguous) into the 128B-swizzled MN-major tile:
+        // queries 32ch .. 32ch+31 are 16B chunks 4ch .. 4ch+3 of row j.
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c8 = 4 * ch + q;  // 8-query chunk index (0..15)
+          const int half = c8 >> 3, chunk = c8 & 7;
+          uint4 w = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+          *reinterpret_cast<uint4*>(ds_row + half * L::kHalfBytes +
+                                    ((chunk ^ (j & 7)) << 4)) = w;
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::kDSFull));
+      ++c;
+    }
+    // epilogue: dV and scale * dK rows of this key tile
+    if (ok) ok = mbar_wait(bar(L::kDKVFull), 0, abort_flag, P.status);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const long long off = (((long long)bt * P.S + kp) * P.Hkv + g) * D;
+    __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(P.dv) + off;
+    __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(P.dk) + off;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t src = tmem + lane_off + 256 + which * D;
+      const float mul = which ? P.scale : 1.f;
+      __nv_bfloat16* dst = which ? dkrow : dvrow;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(src + 32 * ch, o);
+        tmem_wait_ld();
+        uint4 w[4];
+        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float a = c > 0 ? __uint_as_float(o[2 * k]) * mul : 0.f;
+          const float b = c > 0 ? __uint_as_float(o[2 * k + 1]) * mul : 0.f;
+          wp[k] = pack_bf16(a, b);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * ch);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) d4[k] = w[k];
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int qw = warp - 4;
+    const int i = qw * 32 + lane;  // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    int c = 0;
+    while (true) {
+      bool ok = mbar_wait(bar(L::kInfoQ), c & 1, abort_flag, P.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int4 e = info[1];
+      if (e.x == kEnd) break;
+      const int qt = e.x, h = e.y;
+      ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      float* dst = P.dq_acc + (((long long)bt * P.S + qt * kTile + i) * P.Hq + h) * D;
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf) {
+        const uint32_t src = tmem + lane_off + (hf == 0 ? 64 : 128 + 64);
+        uint32_t a[32], b[32];
+        tmem_ld32(src, a);
+        tmem_ld32(src + 32, b);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          red_add_v4(dst + 64 * hf + 4 * k, __uint_as_float(a[4 * k]) * P.scale,
+                     __uint_as_float(a[4 * k + 1]) * P.scale,
+                     __uint_as_float(a[4 * k + 2]) * P.scale,
+                     __uint_as_float(a[4 * k + 3]) * P.scale);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          red_add_v4(dst + 64 * hf + 32 + 4 * k, __uint_as_float(b[4 * k]) * P.scale,
+                     __uint_as_float(b[4 * k + 1]) * P.scale,
+                     __uint_as_float(b[4 * k + 2]) * P.scale,
+                     __uint_as_float(b[4 * k + 3]) * P.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kDQEmpty));
+      ++c;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// dq (bf16) <- dq_acc (fp32), 8 elements per thread-iteration.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src,
+                                                         uint4* __restrict__ dst,
+                                                         long long n8) {
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n8; i += (long long)gridDim.x * 256) {
+    const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
+    dst[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
+                        pack_bf16(b.z, b.w));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
+  auto fn = encode_fn();
+  if (!fn) {
+    fail_cuda_msg("cuTensorMapEncodeTiled", "driver entry point not found");
+    return false;
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)Bt};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                           (cuuint64_t)S * H * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    std::snprintf(msg, sizeof(msg), "CUresult %d", (int)r);
+    fail_cuda_msg("cuTensorMapEncodeTiled", msg);
+    return false;
+  }
+  return true;
+}
+
+template <int D>
+usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
+      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D) || !make_map(&mdo, P.dout, P.Bt, P.S, P.Hq, D))
+    return USP_ERR_CUDA;
+  static int* status = nullptr;
+  if (status == nullptr) {
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_bwd_tc_status);
+    if (e != cudaSuccess) return fail_cuda("cudaGetSymbolAddress(status)", e);
+  }
+  AttnParams Pk = P;
+  Pk.status = status;
+  const int smem = BSmem<D>::kAlloc;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(smem)", e);
+    attr_set = true;
+  }
+  const long long blocks = (long long)(P.S / kTile) * P.Hkv * P.Bt;
+  {
+    ProfScope ps(st, "attn_bwd_tc");
+    attn_bwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv, mdo);
+  }
+  note_launch();
+  usp_status_t r = check_launch();
+  if (r != USP_OK) return r;
+  const long long n8 = (long long)P.Bt * P.S * P.Hq * D / 8;
+  {
+    ProfScope ps(st, "attn_bwd_dq_convert");
+    dq_convert_kernel<<<(unsigned)(n8 < 152LL * 32 * 4 ? (n8 + 255) / 256 : 152 * 16), 256, 0,
+                        st>>>(reinterpret_cast<const float4*>(P.dq_acc),
+                              reinterpret_cast<uint4*>(P.dq), n8);
+  }
+  note_launch();
+  return check_launch();
+}
+
+}  // namespace
+
+int read_clear_bwd_tc_status() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bwd_tc_status, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) cudaMemcpyToSymbol(g_bwd_tc_status, &z, sizeof(int));
+  return v;
+}
+
+bool bwd_tc_supported(const AttnParams& P) {
+  if (P.D != 128 && P.D != 64) return false;
+  if (P.shard % kTile != 0) return false;
+  if (P.layout == kZigzag && P.chunk % kTile != 0) return false;
+  return true;
+}
+
+usp_status_t launch_bwd_tc(const AttnParams& P, cudaStream_t st) {
+  return P.D == 128 ? launch_d<128>(P, st) : launch_d<64>(P, st);
+}
+
 }  // namespace usp

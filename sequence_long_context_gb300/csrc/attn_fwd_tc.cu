@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "tc_ptx.cuh"
+#include "tile_sched.cuh"
 
 namespace usp {
 namespace {
@@ -47,7 +48,7 @@ constexpr int kBN = 128;          // keys per tile
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kEmpty = 0, kFull = 1, kMasked = 2;
+constexpr int kEmpty = kClsEmpty, kMasked = kClsMasked;
 constexpr int kEnd = -1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
@@ -73,69 +74,8 @@ struct Smem {
   static constexpr int kAlloc = kBytes + 1024;          // alignment slack
 };
 
-struct TileSpan {
-  int lo, hi, step;  // natural positions lo, lo+step, ..., hi
-};
-
-__device__ __forceinline__ TileSpan tile_span(const AttnParams& P, int base) {
-  TileSpan t;
-  t.lo = nat_pos(P, base);
-  t.step = (P.layout == kStripe) ? P.cp : 1;
-  t.hi = t.lo + (kBM - 1) * t.step;
-  return t;
-}
-
-// empty / full / masked for one query tile against one key tile. Positions
-// inside each tile are increasing (tiles never cross a chunk), so the tile
-// extremes decide.
-__device__ int classify(const AttnParams& P, const TileSpan& q, const TileSpan& k) {
-  int qlo = q.lo, qhi = q.hi, klo = k.lo, khi = k.hi;
-  if (P.cu != nullptr) {
-    int sq0 = seg_of(P.cu, P.nseq, qlo), sq1 = seg_of(P.cu, P.nseq, qhi);
-    int sk0 = seg_of(P.cu, P.nseq, klo), sk1 = seg_of(P.cu, P.nseq, khi);
-    if (sk1 < sq0 || sk0 > sq1) return kEmpty;
-    if (!(sq0 == sq1 && sk0 == sk1 && sq0 == sk0)) return kMasked;
-    int st = __ldg(P.cu + sq0);
-    qlo -= st; qhi -= st; klo -= st; khi -= st;
-  }
-  if (P.causal && klo > qhi) return kEmpty;
-  bool full = !P.causal || khi <= qlo;
-  if (P.window > 0) {
-    bool any_window = qlo - khi < P.window || !P.causal && khi > qlo;
-    bool any_sink = klo < P.sink;
-    if (!any_window && !any_sink) return kEmpty;
-    bool all_window = qhi - klo < P.window || khi < P.sink;
-    full = full && all_window;
-  }
-  return full ? kFull : kMasked;
-}
-
-// Heavy-first ordering of query-tile pairs (so the hardware block scheduler
-// approximates longest-processing-time-first): causal dense problems visit
-// pairs by decreasing natural position.
-__device__ __forceinline__ int pair_for_rank(const AttnParams& P, int r, int npairs) {
-  if (!P.causal || P.cu != nullptr) return r;
-  if (P.layout == kStripe) {
-    int ppr = P.shard / (2 * kBM);
-    int t_local = ppr - 1 - r / P.cp;
-    int rho = r % P.cp;
-    return rho * ppr + t_local;
-  }
-  int pos = (npairs - 1 - r) * (2 * kBM);
-  if (P.layout == kContiguous) return pos / (2 * kBM);
-  int C = P.chunk, c = pos / C, off = pos - c * C, rho, p;
-  if (c < P.cp) {
-    rho = c;
-    p = rho * P.shard + off;
-  } else {
-    rho = 2 * P.cp - 1 - c;
-    p = rho * P.shard + C + off;
-  }
-  return p / (2 * kBM);
-}
-
-template <int D>
 // 10 warps: three share a 16K-register sub-partition, so <= 168 each.
+template <int D>
 __global__ void __maxnreg__(168)
 attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -154,7 +94,7 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int npairs = P.S / (2 * kBM);
   const int hb = blockIdx.x % (P.Hq * P.Bt);
-  const int pair = pair_for_rank(P, blockIdx.x / (P.Hq * P.Bt), npairs);
+  const int pair = qpair_for_rank(P, blockIdx.x / (P.Hq * P.Bt), npairs);
   const int h = hb / P.Bt, bt = hb % P.Bt;
   const int g = h / P.G;
   const int qbase0 = pair * 2 * kBM;          // permuted row of tile 0
@@ -364,9 +304,15 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           if (!row_visible(rm, ks.lo + j * ks.step))
             sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(sr[0][0]);
+      // row max as 8 independent chains (a single chain is latency-bound)
+      float m8[8];
 #pragma unroll
-      for (int j = 1; j < 128; ++j) mx = fmaxf(mx, __uint_as_float(sr[j >> 5][j & 31]));
+      for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[t >> 5][t & 31]);
+#pragma unroll
+      for (int j = 8; j < 128; ++j)
+        m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       mx *= P.scale_log2;
       // lazy rescale: move the running max only when it grows by > 2^8
       const bool need = mx > m_run + kRescaleThreshold;
@@ -377,7 +323,7 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       }
       l_run *= alpha;
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      float lsum = 0.f;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t pk[32];
@@ -387,12 +333,12 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           const float p0 = ex2(fmaf(__uint_as_float(sr[j0 >> 5][j0 & 31]), P.scale_log2, -msub));
           const float p1 = ex2(fmaf(__uint_as_float(sr[(j0 + 1) >> 5][(j0 + 1) & 31]),
                                     P.scale_log2, -msub));
-          lsum += p0 + p1;
+          ls4[j & 3] += p0 + p1;
           pk[j] = pack_bf16(p0, p1);
         }
         tmem_st32(s_tm + 32 * ch, pk);
       }
-      l_run += lsum;
+      l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       // O_i holds PV of the previous tiles (complete: the commit that
       // signalled S_i tracks every earlier MMA); rescale it to the new max
       // before P_i V is accumulated onto it.

@@ -118,7 +118,8 @@ fwd_simt_kernel(AttnParams P) {
     P.lse[lse_index(P, bt, h, row)] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
-// Delta[bt][h][p] = <dO, O> per row; optionally zeroes the fp32 dQ
+// Delta[bt][h][p] = <dO, O> per row (and, for the tensor-core path, the LSE
+// in log2 units in the same layout); optionally zeroes the fp32 dQ
 // accumulator rows of the same (bt, p, h).
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
@@ -140,7 +141,11 @@ bwd_preprocess_kernel(AttnParams P, int zero_dq) {
 #pragma unroll
     for (int e = 0; e < E; ++e) acc = fmaf(o[e], d[e], acc);
     acc = warp_sum(acc);
-    if (lane == 0) P.delta[((long long)bt * P.Hq + h) * P.S + p] = acc;
+    if (lane == 0) {
+      const long long di = ((long long)bt * P.Hq + h) * P.S + p;
+      P.delta[di] = acc;
+      if (P.lse2 != nullptr) P.lse2[di] = P.lse[lse_index(P, bt, h, p)] * kLog2e;
+    }
     if (zero_dq) {
       float z[E];
 #pragma unroll

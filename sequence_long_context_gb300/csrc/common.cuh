@@ -35,6 +35,7 @@ struct AttnParams {
   float* lse;       // forward: written; backward: read
   const void* dout; // backward only
   float* delta;     // backward: rowsum(dO * O), [Bt][Hq][S]
+  float* lse2;      // backward (tensor-core path): LSE * log2(e), [Bt][Hq][S]
   void* dq;
   void* dk;
   void* dv;
