@@ -175,6 +175,41 @@ size_t usp_attn_bwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
                                    usp_dtype_t dtype, unsigned flags);
 
 /*
+ * usp_attn_bwd_noalloc - usp_attn_bwd for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot provide a workspace: a runtime that has already handed all device
+ * memory to its own pools, or code on a path where cudaMalloc is not
+ * allowed (it may synchronise the device). It computes exactly what
+ * usp_attn_bwd computes, with the same arguments minus the workspace, and
+ * takes its scratch from one fixed 64 MiB array in device memory that the
+ * library declares at file scope. It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *  - Limit: a problem whose usp_attn_bwd_workspace_size (with B = 1 for
+ *    packed batches) exceeds 64 MiB is rejected with USP_ERR_WORKSPACE
+ *    before anything is launched (usp_last_error_detail() says why).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents;
+ *    what must start at zero is cleared on the device at the start of each
+ *    call. Calls that overlap on the GPU (e.g. on two streams) race on the
+ *    array and give wrong results; serialise them.
+ *  - Every GPU that loads the library holds the 64 MiB until process exit.
+ * Errors: as usp_attn_bwd, plus USP_ERR_WORKSPACE for the size limit.
+ */
+usp_status_t usp_attn_bwd_noalloc(const void *q, const void *k, const void *v,
+                                  const void *out, const float *lse,
+                                  const void *dout, void *dq, void *dk,
+                                  void *dv, int B, int S, int Hq, int Hkv,
+                                  int D, float softmax_scale, int causal,
+                                  int window, int sink_tokens,
+                                  const int32_t *cu_seqlens, int cp_size,
+                                  int ulysses_degree, usp_layout_t layout,
+                                  usp_dtype_t dtype, unsigned flags,
+                                  usp_stream_t stream);
+
+/*
  * usp_merge_partials - merge n attention partials with the log-sum-exp rule.
  *
  * "Tree Attention" (Long Context Attention notes): because logsumexp and max

@@ -94,6 +94,21 @@ def usp_attn_bwd_workspace_size(B, S, Hq, Hkv, D, cp_size, ulysses_degree,
         B, S, Hq, Hkv, D, cp_size, ulysses_degree, _enum(DTYPE, dtype), flags))
 
 
+def usp_attn_bwd_noalloc(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv,
+                         D, softmax_scale, causal, window, sink_tokens,
+                         cu_seqlens, cp_size, ulysses_degree, layout, dtype,
+                         flags=0, stream=None) -> None:
+    """usp_attn_bwd without a workspace: scratch comes from the library's
+    fixed 64 MiB device array (for callers that cannot allocate; calls that
+    overlap on the GPU race on it)."""
+    _check(_lib.load().usp_attn_bwd_noalloc(
+        _p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk),
+        _p(dv), B, S, Hq, Hkv, D, float(softmax_scale), int(causal),
+        int(window), int(sink_tokens), _p(cu_seqlens), cp_size,
+        ulysses_degree, _enum(LAYOUT, layout), _enum(DTYPE, dtype), flags,
+        _stream(stream)))
+
+
 def usp_merge_partials(o_parts, lse_parts, n, rows, D, tree_order, o_out,
                        out_dtype, lse_out, stream=None) -> None:
     _check(_lib.load().usp_merge_partials(

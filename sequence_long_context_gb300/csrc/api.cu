@@ -60,6 +60,10 @@ usp_status_t fail_cuda_msg(const char* where, const char* msg) {
   return USP_ERR_CUDA;
 }
 
+void set_error_detail(const char* msg) {
+  std::snprintf(g_detail, sizeof(g_detail), "%s", msg);
+}
+
 usp_status_t fail_cuda(const char* where, cudaError_t e) {
   return fail_cuda_msg(where, cudaGetErrorString(e));
 }

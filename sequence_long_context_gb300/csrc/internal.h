@@ -18,6 +18,8 @@ usp_status_t check_launch();
 // (usp_last_error_detail()); returns USP_ERR_CUDA.
 usp_status_t fail_cuda(const char* where, cudaError_t e);
 usp_status_t fail_cuda_msg(const char* where, const char* msg);
+// Sets the usp_last_error_detail() text without changing any status.
+void set_error_detail(const char* msg);
 
 // Brackets one kernel launch with timing events when the kernel timer is on
 // (usp_profile_enable); a no-op otherwise.
