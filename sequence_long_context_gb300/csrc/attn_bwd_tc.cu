@@ -57,12 +57,19 @@ struct BSmem {
   static constexpr int kBar = kDS + kTile * kTile * 2;
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
-                       kDKVFull = 12, kMmaDone = 13, kNumBars = 14;
-  static constexpr int kSched = kBar + 8 * kNumBars;  // int4 x 2
+                       kDKVFull = 12, kMmaDone = 13, kGroup = 14, kNumBars = 15;
+  // 16-byte aligned: int4 / float4 accesses below
+  static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
   static constexpr int kMisc = kInfo + 32;            // tmem base, abort
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kRowStats = kMisc + 16;        // LSE*log2e, Delta: 2 x 128 fp32
+  static constexpr int kBytes = kRowStats + 2 * kTile * 4;
   static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kSched % 16 == 0 && kInfo % 16 == 0 && kRowStats % 16 == 0,
+                "vector accesses need 16-byte alignment");
+  static_assert(kDS % 1024 == 0 && kQ % 1024 == 0 && kDO % 1024 == 0,
+                "128-byte swizzled tiles need 1024-byte alignment");
+  static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
 };
 
 // Visible query interval of one key (natural positions): a key at position j
@@ -126,6 +133,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
+    mbar_init(bar(L::kGroup), kTile);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -288,8 +296,22 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       const bool masked = e.z == kClsMasked;
       const TileSpan qs = tile_span(P, qt * kTile);
       const long long row_off = ((long long)bt * P.Hq + h) * P.S + (long long)qt * kTile;
-      const float* lse2 = P.lse2 + row_off;
-      const float* delta = P.delta + row_off;
+      // stage this query tile's LSE (log2 units) and Delta in shared memory:
+      // one coalesced load per thread, overlapping the S^T MMA
+      float* lse2 = reinterpret_cast<float*>(sm + L::kRowStats);
+      float* delta = lse2 + kTile;
+      const float my_lse2 = __ldg(P.lse2 + row_off + j);
+      const float my_delta = __ldg(P.delta + row_off + j);
+      // group barrier of the 128 softmax threads (bounded, unlike bar.sync):
+      // the previous tile's readers are done, then the new values are in
+      mbar_arrive(bar(L::kGroup));
+      ok = mbar_wait(bar(L::kGroup), 0, abort_flag, P.status);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      lse2[j] = my_lse2;
+      delta[j] = my_delta;
+      mbar_arrive(bar(L::kGroup));
+      ok = mbar_wait(bar(L::kGroup), 1, abort_flag, P.status);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
       ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -301,7 +323,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         float lv[32];
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(lse2 + 32 * ch) + k4);
+          const float4 x = reinterpret_cast<const float4*>(lse2 + 32 * ch)[k4];
           lv[4 * k4] = x.x; lv[4 * k4 + 1] = x.y; lv[4 * k4 + 2] = x.z; lv[4 * k4 + 3] = x.w;
         }
         tmem_wait_ld();
@@ -334,7 +356,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         float dl[32];
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(delta + 32 * ch) + k4);
+          const float4 x = reinterpret_cast<const float4*>(delta + 32 * ch)[k4];
           dl[4 * k4] = x.x; dl[4 * k4 + 1] = x.y; dl[4 * k4 + 2] = x.z; dl[4 * k4 + 3] = x.w;
         }
         tmem_wait_ld();

@@ -67,11 +67,14 @@ struct Smem {
   static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5,
                        kVEmpty = 7, kSFull = 9, kPFull = 11, kOFull = 13,
                        kInfoFull = 15, kMmaDone = 17, kNumBars = 18;
-  static constexpr int kSched = kBar + 8 * kNumBars;    // int4 x 2
+  static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;             // int2 x 2
   static constexpr int kMisc = kInfo + 16;              // tmem base, abort
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;          // alignment slack
+  static_assert(kSched % 16 == 0 && kInfo % 8 == 0, "vector accesses need alignment");
+  static_assert(kK % 1024 == 0 && kV % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
 };
 
 // 10 warps: three share a 16K-register sub-partition, so <= 168 each.

@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kMaxTreeDepth = 7;  // n <= 64
+constexpr int kRegParts = 8;      // up to this many partials merge in registers
 
 template <int E>
 __device__ __forceinline__ void merge_into(float* oa, float& la, const float* ob,
@@ -59,7 +60,38 @@ merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_pa
     const float* op = o_parts + row * D + lane * E;
     float acc[E];
     float L;
-    if (!tree) {
+    if (n <= kRegParts) {
+      // all partials of the row are loaded at once (n loads in flight) and
+      // merged in registers; indices are static after unrolling
+      float part[kRegParts][E], pl[kRegParts];
+#pragma unroll
+      for (int i = 0; i < kRegParts; ++i) {
+        if (i < n) {
+          load_row<float, E>(op + (long long)i * rows * D, part[i]);
+          pl[i] = __ldg(lse_parts + (long long)i * rows + row);
+          if (pl[i] == -INFINITY) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) part[i][e] = 0.f;
+          }
+        }
+      }
+      if (!tree) {
+#pragma unroll
+        for (int i = 1; i < kRegParts; ++i)
+          if (i < n) merge_into<E>(part[0], pl[0], part[i], pl[i]);
+      } else {
+        // pairwise levels: at stride s, slot i absorbs slot i + s; a slot
+        // without a partner is carried up unchanged
+#pragma unroll
+        for (int s = 1; s < kRegParts; s *= 2)
+#pragma unroll
+          for (int i = 0; i + s < kRegParts; i += 2 * s)
+            if (i + s < n) merge_into<E>(part[i], pl[i], part[i + s], pl[i + s]);
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = part[0][e];
+      L = pl[0];
+    } else if (!tree) {
       load_row<float, E>(op, acc);
       L = __ldg(lse_parts + row);
       if (L == -INFINITY) {

@@ -18,9 +18,8 @@ namespace usp {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVecPerThread = 4;
 
-int grid_for(long long work_items) {
+int grid_for(long long warp_units) {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -28,80 +27,64 @@ int grid_for(long long work_items) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
   }
-  long long per_block = (long long)kThreads * kVecPerThread;
-  long long need = (work_items + per_block - 1) / per_block;
+  constexpr long long kWarpsPerBlock = kThreads / 32;
+  long long need = (warp_units + kWarpsPerBlock - 1) / kWarpsPerBlock;
   long long cap = (long long)sms * 8;  // 8 resident 256-thread blocks per SM
   return (int)(need < cap ? (need < 1 ? 1 : need) : cap);
 }
 
-// dst row p <- src row nat(p) (extract) or dst row nat(p) <- src row p.
+// One warp copies one contiguous run of n 16-byte vectors, four per lane in
+// flight.
+__device__ __forceinline__ void warp_copy(const uint4* __restrict__ s,
+                                          uint4* __restrict__ d, unsigned n,
+                                          unsigned lane) {
+  unsigned c = lane;
+  for (; c + 96 < n; c += 128) {
+    const uint4 a = __ldg(s + c), b = __ldg(s + c + 32), e = __ldg(s + c + 64),
+                f = __ldg(s + c + 96);
+    d[c] = a;
+    d[c + 32] = b;
+    d[c + 64] = e;
+    d[c + 96] = f;
+  }
+  for (; c < n; c += 32) d[c] = __ldg(s + c);
+}
+
+// Token row p of the rank-major tensor <-> token row nat(p) of the natural
+// tensor; a row (H*D elements) is rv vectors. One warp per row.
 __global__ void __launch_bounds__(kThreads)
 permute_layout_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                       unsigned rows, unsigned S, unsigned rv, int layout,
                       int cp, int shard, int chunk, int restore) {
-  const unsigned total = rows * rv;
-  const unsigned stride = gridDim.x * blockDim.x;
-  unsigned f = blockIdx.x * blockDim.x + threadIdx.x;
-  for (; f < total; f += stride * kVecPerThread) {
-    uint4 val[kVecPerThread];
-    unsigned dsti[kVecPerThread];
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      unsigned g = f + u * stride;
-      if (g < total) {
-        unsigned r = g / rv, c = g - r * rv;
-        unsigned b = r / S, p = r - b * S;
-        unsigned np = (unsigned)nat_pos((int)p, layout, cp, shard, chunk);
-        unsigned a = (b * S + np) * rv + c;
-        if (restore) {
-          val[u] = __ldg(src + g);
-          dsti[u] = a;
-        } else {
-          val[u] = __ldg(src + a);
-          dsti[u] = g;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      unsigned g = f + u * stride;
-      if (g < total) dst[dsti[u]] = val[u];
-    }
+  const unsigned lane = threadIdx.x & 31;
+  const unsigned nwarps = gridDim.x * (kThreads / 32);
+  for (unsigned r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < rows;
+       r += nwarps) {
+    const unsigned b = r / S, p = r - b * S;
+    const unsigned other = b * S + (unsigned)nat_pos((int)p, layout, cp, shard, chunk);
+    const size_t so = (size_t)(restore ? r : other) * rv;
+    const size_t dof = (size_t)(restore ? other : r) * rv;
+    warp_copy(src + so, dst + dof, rv, lane);
   }
 }
 
-// Ulysses: src [B][S][ud*rvu] <-> dst [ud][B][S][rvu] (16-byte vectors).
+// Ulysses exchange: src [B*S][ud][rvu] <-> dst [ud][B*S][rvu] (16-byte
+// vectors); one warp per (group, token row).
 __global__ void __launch_bounds__(kThreads)
 ulysses_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                unsigned BS, unsigned rvu, unsigned ud, int seq2head) {
-  const unsigned total = BS * rvu * ud;
-  const unsigned stride = gridDim.x * blockDim.x;
-  unsigned f = blockIdx.x * blockDim.x + threadIdx.x;
-  for (; f < total; f += stride * kVecPerThread) {
-    uint4 val[kVecPerThread];
-    unsigned dsti[kVecPerThread];
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      unsigned g = f + u * stride;  // index in the head-grouped tensor
-      if (g < total) {
-        unsigned grp = g / (BS * rvu);
-        unsigned rem = g - grp * (BS * rvu);
-        unsigned r = rem / rvu, c = rem - r * rvu;
-        unsigned a = (r * ud + grp) * rvu + c;  // index in [B][S][H] order
-        if (seq2head) {
-          val[u] = __ldg(src + a);
-          dsti[u] = g;
-        } else {
-          val[u] = __ldg(src + g);
-          dsti[u] = a;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      unsigned g = f + u * stride;
-      if (g < total) dst[dsti[u]] = val[u];
-    }
+  const unsigned lane = threadIdx.x & 31;
+  const unsigned nwarps = gridDim.x * (kThreads / 32);
+  const unsigned units = BS * ud;
+  for (unsigned t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < units;
+       t += nwarps) {
+    const unsigned grp = t / BS, r = t - grp * BS;
+    const size_t grouped = (size_t)(grp * BS + r) * rvu;  // [ud][B*S] order
+    const size_t flat = (size_t)(r * ud + grp) * rvu;     // [B*S][ud] order
+    if (seq2head)
+      warp_copy(src + flat, dst + grouped, rvu, lane);
+    else
+      warp_copy(src + grouped, dst + flat, rvu, lane);
   }
 }
 
@@ -112,13 +95,12 @@ usp_status_t launch_permute_layout(const void* src, void* dst, int B, int S,
                                    int restore, cudaStream_t st) {
   unsigned rv = (unsigned)(row_bytes / 16);
   unsigned rows = (unsigned)B * (unsigned)S;
-  long long total = (long long)rows * rv;
-  if (total == 0) return USP_OK;
+  if ((long long)rows * rv == 0) return USP_OK;
   int shard = S / cp;
   int chunk = layout == kZigzag ? S / (2 * cp) : shard;
   {
     ProfScope ps(st, "permute_layout");
-    permute_layout_kernel<<<grid_for(total), kThreads, 0, st>>>(
+    permute_layout_kernel<<<grid_for(rows), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
         rows, (unsigned)S, rv, layout, cp, shard, chunk, restore);
   }
@@ -131,11 +113,10 @@ usp_status_t launch_ulysses(const void* src, void* dst, int B, int S,
                             cudaStream_t st) {
   unsigned rvu = (unsigned)(row_bytes / ud / 16);
   unsigned BS = (unsigned)B * (unsigned)S;
-  long long total = (long long)BS * rvu * ud;
-  if (total == 0) return USP_OK;
+  if ((long long)BS * rvu * ud == 0) return USP_OK;
   {
     ProfScope ps(st, "permute_ulysses");
-    ulysses_kernel<<<grid_for(total), kThreads, 0, st>>>(
+    ulysses_kernel<<<grid_for((long long)BS * ud), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
         BS, rvu, (unsigned)ud, seq2head);
   }
