@@ -17,8 +17,10 @@
 //              dS^T = P^T (dP^T - Delta); P^T and dS^T go back to tensor
 //              memory as bf16 (A operands of dV and dK) and dS to shared
 //              memory (A operand of dQ)
-//   warps 4-7  dQ group, one query row per thread: drains the dQ tile from
-//              tensor memory into the global accumulator
+//   warps 4-7  dQ group, one query row per thread: takes the dQ tile out of
+//              tensor memory (freeing it for the next tile), transposes it
+//              through the dS buffer and adds it into the global fp32
+//              accumulator with reductions that each cover whole cache lines
 //   warp 8     producer: K, V once; then Q, dO tiles through a 2-slot ring
 //   warp 9     MMA issuer and tensor-memory owner
 // Tensor memory (512 columns): S^T [0,128) with P^T over its first 64 and
@@ -57,7 +59,8 @@ struct BSmem {
   static constexpr int kBar = kDS + kTile * kTile * 2;
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
-                       kDKVFull = 12, kMmaDone = 13, kGroup = 14, kNumBars = 15;
+                       kDKVFull = 12, kMmaDone = 13, kGroup = 14, kDQGroup = 15,
+                       kDSFree = 16, kNumBars = 17;
   // 16-byte aligned: int4 / float4 accesses below
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
@@ -126,9 +129,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     }
     mbar_init(bar(L::kSFull), 1);
     mbar_init(bar(L::kDPFull), 1);
-    mbar_init(bar(L::kDSFull), kTile);
+    mbar_init(bar(L::kDSFull), kTile / 32);   // one arrival per softmax warp
     mbar_init(bar(L::kDQFull), 1);
-    mbar_init(bar(L::kDQEmpty), kTile);
+    mbar_init(bar(L::kDQEmpty), kTile / 32);  // one arrival per drain warp
+    mbar_init(bar(L::kDQGroup), kTile);
+    mbar_init(bar(L::kDSFree), kTile / 32);
     mbar_init(bar(L::kInfoS), 1);
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
@@ -343,8 +348,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         tmem_st16(t_s + 16 * ch, pk);
       }
       ok = mbar_wait(bar(L::kDPFull), c & 1, abort_flag, P.status);
-      // dS in shared memory is still read by the previous tile's dQ MMAs
-      if (ok && c > 0) ok = mbar_wait(bar(L::kDQFull), (c - 1) & 1, abort_flag, P.status);
+      // the dS buffer is still used by the previous tile (its dQ MMAs, then
+      // the dQ drain staging through it)
+      if (ok && c > 0) ok = mbar_wait(bar(L::kDSFree), (c - 1) & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       tmem_wait_st();
@@ -384,7 +390,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(L::kDSFull));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kDSFull));
       ++c;
     }
     // epilogue: dV and scale * dK rows of this key tile
@@ -423,6 +430,12 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     const int i = qw * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     int c = 0;
+    int gq = 0;  // uses of the dQ group barrier so far
+    // bounded barrier of the 128 drain threads (parity of the use count)
+    auto group_sync = [&](int b, int use) -> bool {
+      mbar_arrive(bar(b));
+      return __all_sync(0xffffffffu, mbar_wait(bar(b), use & 1, abort_flag, P.status));
+    };
     while (true) {
       bool ok = mbar_wait(bar(L::kInfoQ), c & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -432,29 +445,49 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      float* dst = P.dq_acc + (((long long)bt * P.S + qt * kTile + i) * P.Hq + h) * D;
+      // 1. both dQ halves into registers; the tensor-memory columns are then
+      //    free for the next tile's S^T and dP^T
+      uint32_t dqv[D / 64][64];
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
         const uint32_t src = tmem + lane_off + (hf == 0 ? 64 : 128 + 64);
-        uint32_t a[32], b[32];
-        tmem_ld32(src, a);
-        tmem_ld32(src + 32, b);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          red_add_v4(dst + 64 * hf + 4 * k, __uint_as_float(a[4 * k]) * P.scale,
-                     __uint_as_float(a[4 * k + 1]) * P.scale,
-                     __uint_as_float(a[4 * k + 2]) * P.scale,
-                     __uint_as_float(a[4 * k + 3]) * P.scale);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          red_add_v4(dst + 64 * hf + 32 + 4 * k, __uint_as_float(b[4 * k]) * P.scale,
-                     __uint_as_float(b[4 * k + 1]) * P.scale,
-                     __uint_as_float(b[4 * k + 2]) * P.scale,
-                     __uint_as_float(b[4 * k + 3]) * P.scale);
+        tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(&dqv[hf][0]));
+        tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(&dqv[hf][32]));
       }
+      tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(L::kDQEmpty));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kDQEmpty));
+      // 2. per half: rows -> shared memory (the dS buffer, whose dQ readers
+      //    have finished), then read back with 16 lanes per 256-byte row
+      //    segment so each reduction instruction covers whole cache lines.
+      //    16-byte chunk j of row r lives at chunk j ^ (r & 15).
+      float* stage = reinterpret_cast<float*>(sm + L::kDS);
+      float* rows_base = P.dq_acc + (((long long)bt * P.S + qt * kTile) * P.Hq + h) * D;
+      const long long row_stride = (long long)P.Hq * D;
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf) {
+        if (!(ok = group_sync(L::kDQGroup, gq++))) break;  // buffer free
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          *reinterpret_cast<uint4*>(stage + i * 64 + ((j ^ (i & 15)) << 2)) =
+              make_uint4(dqv[hf][4 * j], dqv[hf][4 * j + 1], dqv[hf][4 * j + 2],
+                         dqv[hf][4 * j + 3]);
+        if (!(ok = group_sync(L::kDQGroup, gq++))) break;  // rows written
+        const int cj = lane & 15;  // 16-byte chunk of the row
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += 2) {
+          const int r = qw * 32 + rr + (lane >> 4);
+          const float4 x = *reinterpret_cast<const float4*>(stage + r * 64 +
+                                                           ((cj ^ (r & 15)) << 2));
+          red_add_v4(rows_base + r * row_stride + 64 * hf + 4 * cj, x.x * P.scale,
+                     x.y * P.scale, x.z * P.scale, x.w * P.scale);
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // 3. this warp no longer reads the buffer: the next tile's dS may go in
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kDSFree));
       ++c;
     }
   }

@@ -112,7 +112,7 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       mbar_init(bar(L::kVFull + s), 1);
       mbar_init(bar(L::kVEmpty + s), 1);
       mbar_init(bar(L::kSFull + s), 1);
-      mbar_init(bar(L::kPFull + s), kBM);
+      mbar_init(bar(L::kPFull + s), kBM / 32);  // one arrival per softmax warp
       mbar_init(bar(L::kOFull + s), 1);
       mbar_init(bar(L::kInfoFull + s), 1);
     }
@@ -326,22 +326,37 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       }
       l_run *= alpha;
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = exp2(s * scale_log2 - m): scale-and-subtract and the row sum run
+      // on packed fp32 pairs (one FMA-pipe instruction per two elements)
+      const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
+      const uint64_t nm2 = f2_pack(-msub, -msub);
+      uint64_t ls2[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int j0 = 64 * ch + 2 * j;
-          const float p0 = ex2(fmaf(__uint_as_float(sr[j0 >> 5][j0 & 31]), P.scale_log2, -msub));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[(j0 + 1) >> 5][(j0 + 1) & 31]),
-                                    P.scale_log2, -msub));
-          ls4[j & 3] += p0 + p1;
+          const uint64_t x = f2_fma(
+              f2_pack(__uint_as_float(sr[j0 >> 5][j0 & 31]),
+                      __uint_as_float(sr[(j0 + 1) >> 5][(j0 + 1) & 31])),
+              sc2, nm2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          ls2[j & 3] = f2_add(ls2[j & 3], f2_pack(p0, p1));
           pk[j] = pack_bf16(p0, p1);
         }
         tmem_st32(s_tm + 32 * ch, pk);
       }
-      l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+      {
+        float a0, a1, b0, b1, c0, c1, d0, d1;
+        f2_unpack(ls2[0], a0, a1);
+        f2_unpack(ls2[1], b0, b1);
+        f2_unpack(ls2[2], c0, c1);
+        f2_unpack(ls2[3], d0, d1);
+        l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+      }
       // O_i holds PV of the previous tiles (complete: the commit that
       // signalled S_i tracks every earlier MMA); rescale it to the new max
       // before P_i V is accumulated onto it.
@@ -359,7 +374,8 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::kPFull + i));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kPFull + i));  // one arrival per warp
       ++c;
     }
     // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2
