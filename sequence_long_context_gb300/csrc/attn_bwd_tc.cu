@@ -23,9 +23,9 @@
 //              accumulator with reductions that each cover whole cache lines
 //   warp 8     producer: K, V once; then Q, dO tiles through a 2-slot ring
 //   warp 9     MMA issuer and tensor-memory owner
-// Tensor memory (512 columns): S^T [0,128) with P^T over its first 64 and
-// dQ[:, :64] over its last 64; dP^T [128,256) with dS^T over its first 64 and
-// dQ[:, 64:] over its last 64; dV [256, 256+D); dK [256+D, 256+2D).
+// Tensor memory (512 columns): S^T [0,128), overwritten by P^T (bf16, first
+// 64 columns) and dS^T (bf16, last 64); dP^T [128,256), overwritten by dQ
+// (fp32, D columns); dV [256, 256+D); dK [256+D, 256+2D).
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -207,12 +207,15 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // Per query tile n: S^T = K Q^T, dP^T = V dO^T; after dS is ready:
-    // dQ = dS K (both D halves), then dV += P^T dO, dK += dS^T Q. The next
-    // S^T/dP^T overwrite the dQ columns, so they wait until dQ is drained.
+    // Per query tile n: S^T = K Q^T into [0,128); dP^T = V dO^T into
+    // [128,256) once the previous tile's dQ has been taken out of those
+    // columns; when dS is ready: dQ = dS K into [128,256) as one N=D block,
+    // then dV += P^T dO (P^T as bf16 over S^T's first 64 columns) and
+    // dK += dS^T Q (dS^T as bf16 over S^T's last 64). The next S^T only has
+    // to follow this tile's dV/dK in issue order, never the dQ drain.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, 0, 0);
-      constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, 64, 1, 1);
+      constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, D, 1, 1);
       constexpr uint32_t kIdKV = idesc_bf16_f32(kTile, D, 0, 1);
       const uint32_t t_s = tmem, t_dp = tmem + 128;
       const uint32_t t_dv = tmem + 256, t_dk = tmem + 256 + D;
@@ -224,13 +227,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         if (!(ok = mbar_wait(bar(L::kQFull + slot), use & 1, abort_flag, P.status))) break;
         const int4 e = sched[slot];
         if (e.x == kEnd) break;
-        if (n > 0 && !(ok = mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status)))
-          break;
         tc_fence_after();
         info[0] = e;
         mbar_arrive(bar(L::kInfoS));
-        info[1] = e;
-        mbar_arrive(bar(L::kInfoQ));
         const uint32_t qa = sbase + L::kQ + slot * L::kTileBytes;
         const uint32_t doa = sbase + L::kDO + slot * L::kTileBytes;
 #pragma unroll
@@ -240,6 +239,13 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kSFull));
+        // the previous dQ must have left [128,256) (and the drain must have
+        // read its entry) before dP^T and the next drain entry
+        if (n > 0 && !(ok = mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status)))
+          break;
+        tc_fence_after();
+        info[1] = e;
+        mbar_arrive(bar(L::kInfoQ));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
@@ -249,15 +255,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         mma_commit(bar(L::kDPFull));
         if (!(ok = mbar_wait(bar(L::kDSFull), n & 1, abort_flag, P.status))) break;
         tc_fence_after();
-        // dQ[:, 64 hf : 64 hf + 64] = dS K[:, 64 hf : ...]  (K dim = keys)
-        for (int hf = 0; hf < L::kHalves; ++hf) {
-          const uint32_t dst = hf == 0 ? t_s + 64 : t_dp + 64;
+        // dQ = dS K (M = queries, K dim = keys; both operands MN-major)
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(dst, sdesc_sw128(dsa + kk * 2048, L::kHalfBytes, 1024),
-                   sdesc_sw128(ka + hf * L::kHalfBytes + kk * 2048, L::kHalfBytes, 1024),
-                   kIdDQ, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(t_dp, sdesc_sw128(dsa + kk * 2048, L::kHalfBytes, 1024),
+                 sdesc_sw128(ka + kk * 2048, L::kHalfBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
         mma_commit(bar(L::kDQFull));
         // dV += P^T dO ; dK += dS^T Q  (K dim = queries; A from tensor memory)
 #pragma unroll
@@ -266,8 +268,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                  (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dk, t_dp + kk * 8, sdesc_sw128(qa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
-                 (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(t_dk, t_s + 64 + kk * 8, sdesc_sw128(qa + kk * 2048, L::kHalfBytes, 1024),
+                 kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kQEmpty + slot));
         ++n;
       }
@@ -375,7 +377,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           const float d1 = pf.y * (__uint_as_float(dv[2 * k + 1]) - dl[2 * k + 1]);
           dk[k] = pack_bf16(d0, d1);
         }
-        tmem_st16(t_dp + 16 * ch, dk);
+        tmem_st16(t_s + 64 + 16 * ch, dk);  // dS^T over S^T's dead second half
         // dS (queries contiguous) into the 128B-swizzled MN-major tile:
         // queries 32ch .. 32ch+31 are 16B chunks 4ch .. 4ch+3 of row j.
 #pragma unroll
@@ -450,7 +452,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       uint32_t dqv[D / 64][64];
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
-        const uint32_t src = tmem + lane_off + (hf == 0 ? 64 : 128 + 64);
+        const uint32_t src = tmem + lane_off + 128 + 64 * hf;
         tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(&dqv[hf][0]));
         tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(&dqv[hf][32]));
       }
