@@ -12,20 +12,23 @@
 // written once (the shard's ring return). dQ contributions are added into an
 // fp32 accumulator in global memory with vector reductions.
 //
-// Roles (320 threads):
-//   warps 0-3  softmax group, one key row per thread: P^T = exp2(S^T - LSE),
+// Roles (448 threads):
+//   warps 0-7  softmax groups, two threads per key row (each owns 64 of the
+//              128 query columns): P^T = exp2(S^T - LSE),
 //              dS^T = P^T (dP^T - Delta); P^T and dS^T go back to tensor
 //              memory as bf16 (A operands of dV and dK) and dS to shared
 //              memory (A operand of dQ)
-//   warps 4-7  dQ group, one query row per thread: takes the dQ tile out of
+//   warps 8-11 dQ group, one query row per thread: takes the dQ tile out of
 //              tensor memory (freeing it for the next tile), transposes it
 //              through the dS buffer and adds it into the global fp32
 //              accumulator with reductions that each cover whole cache lines
-//   warp 8     producer: K, V once; then Q, dO tiles through a 2-slot ring
-//   warp 9     MMA issuer and tensor-memory owner
-// Tensor memory (512 columns): S^T [0,128), overwritten by P^T (bf16, first
-// 64 columns) and dS^T (bf16, last 64); dP^T [128,256), overwritten by dQ
-// (fp32, D columns); dV [256, 256+D); dK [256+D, 256+2D).
+//   warp 12    producer: K, V once; then Q, dO tiles through a 2-slot ring
+//   warp 13    MMA issuer and tensor-memory owner
+// Tensor memory (512 columns): S^T [0,128); queries 64g..64g+63 (softmax
+// group g) live in columns [64g, 64g+64) and are overwritten in place by
+// their P^T (bf16 pairs, first 32 columns) and dS^T (last 32); dP^T
+// [128,256), overwritten by dQ (fp32, D columns); dV [256, 256+D);
+// dK [256+D, 256+2D).
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -41,9 +44,10 @@ using namespace tc;
 
 __device__ int g_bwd_tc_status = 0;
 
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 448;
+constexpr int kDrainWarp0 = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr int kEnd = -1;
 
 template <int D>
@@ -96,8 +100,9 @@ __device__ __forceinline__ ColMask col_mask(const AttnParams& P, int j) {
   return m;
 }
 
+// 14 warps: four share a 16K-register sub-partition, so <= 128 each.
 template <int D>
-__global__ void __maxnreg__(168)
+__global__ void __maxnreg__(128)
 attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
@@ -129,7 +134,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     }
     mbar_init(bar(L::kSFull), 1);
     mbar_init(bar(L::kDPFull), 1);
-    mbar_init(bar(L::kDSFull), kTile / 32);   // one arrival per softmax warp
+    mbar_init(bar(L::kDSFull), 2 * kTile / 32);  // one arrival per softmax warp
     mbar_init(bar(L::kDQFull), 1);
     mbar_init(bar(L::kDQEmpty), kTile / 32);  // one arrival per drain warp
     mbar_init(bar(L::kDQGroup), kTile);
@@ -138,7 +143,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
-    mbar_init(bar(L::kGroup), kTile);
+    mbar_init(bar(L::kGroup), 2 * kTile);  // all 256 softmax threads
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -210,8 +215,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     // Per query tile n: S^T = K Q^T into [0,128); dP^T = V dO^T into
     // [128,256) once the previous tile's dQ has been taken out of those
     // columns; when dS is ready: dQ = dS K into [128,256) as one N=D block,
-    // then dV += P^T dO (P^T as bf16 over S^T's first 64 columns) and
-    // dK += dS^T Q (dS^T as bf16 over S^T's last 64). The next S^T only has
+    // then dV += P^T dO and dK += dS^T Q with P^T / dS^T read as bf16 from
+    // the S^T columns (16 queries per MMA). The next S^T only has
     // to follow this tile's dV/dK in issue order, never the dQ drain.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, 0, 0);
@@ -264,12 +269,14 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         // dV += P^T dO ; dK += dS^T Q  (K dim = queries; A from tensor memory)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dv, t_s + kk * 8, sdesc_sw128(doa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
+          mma_ts(t_dv, t_s + 8 * kk + 32 * (kk >> 2),
+                 sdesc_sw128(doa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
                  (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dk, t_s + 64 + kk * 8, sdesc_sw128(qa + kk * 2048, L::kHalfBytes, 1024),
-                 kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(t_dk, t_s + 32 + 8 * kk + 32 * (kk >> 2),
+                 sdesc_sw128(qa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
+                 (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kQEmpty + slot));
         ++n;
       }
@@ -284,14 +291,20 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       mma_commit(bar(L::kMmaDone));
       mbar_wait(bar(L::kMmaDone), 0, abort_flag, P.status);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    const int j = warp * 32 + lane;  // key row = TMEM lane
-    const int kp = kt * kTile + j;   // permuted key row
+    // Two groups share each key row: group `half` owns query columns
+    // [64 half, 64 half + 64) of S^T, dP^T, P^T, dS^T and of the dS tile.
+    const int half = warp >> 2, quarter = warp & 3;
+    const int j = quarter * 32 + lane;  // key row = TMEM lane
+    const int kp = kt * kTile + j;      // permuted key row
     const ColMask cm = col_mask(P, nat_pos(P, kp));
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
     uint8_t* ds_row = sm + L::kDS + j * 128;
+    float* lse2 = reinterpret_cast<float*>(sm + L::kRowStats);
+    float* delta = lse2 + kTile;
+    const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
     int c = 0;
     bool ok = true;
     while (true) {
@@ -303,28 +316,27 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       const bool masked = e.z == kClsMasked;
       const TileSpan qs = tile_span(P, qt * kTile);
       const long long row_off = ((long long)bt * P.Hq + h) * P.S + (long long)qt * kTile;
-      // stage this query tile's LSE (log2 units) and Delta in shared memory:
-      // one coalesced load per thread, overlapping the S^T MMA
-      float* lse2 = reinterpret_cast<float*>(sm + L::kRowStats);
-      float* delta = lse2 + kTile;
-      const float my_lse2 = __ldg(P.lse2 + row_off + j);
-      const float my_delta = __ldg(P.delta + row_off + j);
-      // group barrier of the 128 softmax threads (bounded, unlike bar.sync):
-      // the previous tile's readers are done, then the new values are in
+      // stage this query tile's LSE (log2 units, loaded by group 0) and Delta
+      // (group 1) in shared memory, overlapping the S^T MMA. A bounded group
+      // barrier of the 256 softmax threads: the previous tile's readers are
+      // done, then the new values are in.
+      const float mine = __ldg((half == 0 ? P.lse2 : P.delta) + row_off + j);
       mbar_arrive(bar(L::kGroup));
       ok = mbar_wait(bar(L::kGroup), 0, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      lse2[j] = my_lse2;
-      delta[j] = my_delta;
+      (half == 0 ? lse2 : delta)[j] = mine;
       mbar_arrive(bar(L::kGroup));
       ok = mbar_wait(bar(L::kGroup), 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // P^T row (queries along columns) -> bf16 pairs into S^T columns [0, 64)
+      // P^T (queries along columns) -> bf16 pairs. Each group writes only
+      // into its own 64 S^T columns (P^T over the first 32, later dS^T over
+      // the last 32), so the groups never touch each other's columns.
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * half + cc;
         uint32_t sv[32];
         tmem_ld32(t_s + 32 * ch, sv);
         float lv[32];
@@ -337,8 +349,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          float p0 = ex2(fmaf(__uint_as_float(sv[2 * k]), P.scale_log2, -lv[2 * k]));
-          float p1 = ex2(fmaf(__uint_as_float(sv[2 * k + 1]), P.scale_log2, -lv[2 * k + 1]));
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
+                                    sc2, f2_pack(-lv[2 * k], -lv[2 * k + 1]));
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
           if (masked) {
             const int i0 = qs.lo + (32 * ch + 2 * k) * qs.step;
             const int i1 = i0 + qs.step;
@@ -347,7 +362,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           }
           pk[k] = pack_bf16(p0, p1);
         }
-        tmem_st16(t_s + 16 * ch, pk);
+        tmem_st16(t_s + 64 * half + 16 * cc, pk);  // own columns, already read
       }
       ok = mbar_wait(bar(L::kDPFull), c & 1, abort_flag, P.status);
       // the dS buffer is still used by the previous tile (its dQ MMAs, then
@@ -357,10 +372,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tc_fence_after();
       tmem_wait_st();
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * half + cc;
         uint32_t dv[32], pv[16];
         tmem_ld32(t_dp + 32 * ch, dv);
-        tmem_ld16(t_s + 16 * ch, pv);
+        tmem_ld16(t_s + 64 * half + 16 * cc, pv);
         float dl[32];
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
@@ -373,20 +389,23 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         for (int k = 0; k < 16; ++k) {
           __nv_bfloat162 pp = *reinterpret_cast<__nv_bfloat162*>(&pv[k]);
           const float2 pf = __bfloat1622float2(pp);
-          const float d0 = pf.x * (__uint_as_float(dv[2 * k]) - dl[2 * k]);
-          const float d1 = pf.y * (__uint_as_float(dv[2 * k + 1]) - dl[2 * k + 1]);
+          // dS = P dP - P Delta on packed pairs
+          const uint64_t p2 = f2_pack(pf.x, pf.y);
+          const uint64_t ds2 = f2_fma(p2, f2_pack(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1])),
+                                      f2_pack(-pf.x * dl[2 * k], -pf.y * dl[2 * k + 1]));
+          float d0, d1;
+          f2_unpack(ds2, d0, d1);
           dk[k] = pack_bf16(d0, d1);
         }
-        tmem_st16(t_s + 64 + 16 * ch, dk);  // dS^T over S^T's dead second half
+        tmem_st16(t_s + 64 * half + 32 + 16 * cc, dk);  // own dead S^T columns
         // dS (queries contiguous) into the 128B-swizzled MN-major tile:
         // queries 32ch .. 32ch+31 are 16B chunks 4ch .. 4ch+3 of row j.
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int c8 = 4 * ch + q;  // 8-query chunk index (0..15)
-          const int half = c8 >> 3, chunk = c8 & 7;
+          const int mh = c8 >> 3, chunk = c8 & 7;
           uint4 w = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
-          *reinterpret_cast<uint4*>(ds_row + half * L::kHalfBytes +
-                                    ((chunk ^ (j & 7)) << 4)) = w;
+          *reinterpret_cast<uint4*>(ds_row + mh * L::kHalfBytes + ((chunk ^ (j & 7)) << 4)) = w;
         }
       }
       tmem_wait_st();
@@ -396,39 +415,34 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) mbar_arrive(bar(L::kDSFull));
       ++c;
     }
-    // epilogue: dV and scale * dK rows of this key tile
+    // epilogue: group 0 writes dV, group 1 writes scale * dK for its key row
     if (ok) ok = mbar_wait(bar(L::kDKVFull), 0, abort_flag, P.status);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     const long long off = (((long long)bt * P.S + kp) * P.Hkv + g) * D;
-    __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(P.dv) + off;
-    __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(P.dk) + off;
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(half ? P.dk : P.dv) + off;
+    const uint32_t src = tmem + lane_off + 256 + half * D;
+    const float mul = half ? P.scale : 1.f;
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t src = tmem + lane_off + 256 + which * D;
-      const float mul = which ? P.scale : 1.f;
-      __nv_bfloat16* dst = which ? dkrow : dvrow;
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t o[32];
+      tmem_ld32(src + 32 * ch, o);
+      tmem_wait_ld();
+      uint4 w[4];
+      uint32_t* wp = reinterpret_cast<uint32_t*>(w);
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(src + 32 * ch, o);
-        tmem_wait_ld();
-        uint4 w[4];
-        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float a = c > 0 ? __uint_as_float(o[2 * k]) * mul : 0.f;
-          const float b = c > 0 ? __uint_as_float(o[2 * k + 1]) * mul : 0.f;
-          wp[k] = pack_bf16(a, b);
-        }
-        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * ch);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) d4[k] = w[k];
+      for (int k = 0; k < 16; ++k) {
+        const float a = c > 0 ? __uint_as_float(o[2 * k]) * mul : 0.f;
+        const float b = c > 0 ? __uint_as_float(o[2 * k + 1]) * mul : 0.f;
+        wp[k] = pack_bf16(a, b);
       }
+      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * ch);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) d4[k] = w[k];
     }
   } else {
     // ------------------------------------------------------------ dQ drain
-    const int qw = warp - 4;
+    const int qw = warp - kDrainWarp0;
     const int i = qw * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     int c = 0;
@@ -437,6 +451,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     auto group_sync = [&](int b, int use) -> bool {
       mbar_arrive(bar(b));
       return __all_sync(0xffffffffu, mbar_wait(bar(b), use & 1, abort_flag, P.status));
+    };
+    auto load_half = [&](int hf, uint32_t (&v)[64]) {
+      const uint32_t src = tmem + lane_off + 128 + 64 * hf;
+      tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_wait_ld();
+    };
+    auto release_tmem = [&]() {  // every dQ column has been read
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kDQEmpty));
     };
     while (true) {
       bool ok = mbar_wait(bar(L::kInfoQ), c & 1, abort_flag, P.status);
@@ -447,34 +472,29 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // 1. both dQ halves into registers; the tensor-memory columns are then
-      //    free for the next tile's S^T and dP^T
-      uint32_t dqv[D / 64][64];
-#pragma unroll
-      for (int hf = 0; hf < D / 64; ++hf) {
-        const uint32_t src = tmem + lane_off + 128 + 64 * hf;
-        tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(&dqv[hf][0]));
-        tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(&dqv[hf][32]));
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kDQEmpty));
-      // 2. per half: rows -> shared memory (the dS buffer, whose dQ readers
-      //    have finished), then read back with 16 lanes per 256-byte row
-      //    segment so each reduction instruction covers whole cache lines.
-      //    16-byte chunk j of row r lives at chunk j ^ (r & 15).
+      // Per 64-column half of dQ: rows -> shared memory (the dS buffer, whose
+      // dQ readers have finished), then read back with 16 lanes per 256-byte
+      // row segment so each reduction instruction covers whole cache lines.
+      // 16-byte chunk j of row r lives at chunk j ^ (r & 15). The next half
+      // is taken out of tensor memory while the current one is reduced, and
+      // the columns are released as soon as all of them have been read.
       float* stage = reinterpret_cast<float*>(sm + L::kDS);
       float* rows_base = P.dq_acc + (((long long)bt * P.S + qt * kTile) * P.Hq + h) * D;
       const long long row_stride = (long long)P.Hq * D;
+      uint32_t v[64];
+      load_half(0, v);
+      if (D == 64) release_tmem();
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
         if (!(ok = group_sync(L::kDQGroup, gq++))) break;  // buffer free
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          *reinterpret_cast<uint4*>(stage + i * 64 + ((j ^ (i & 15)) << 2)) =
-              make_uint4(dqv[hf][4 * j], dqv[hf][4 * j + 1], dqv[hf][4 * j + 2],
-                         dqv[hf][4 * j + 3]);
+        for (int q = 0; q < 16; ++q)
+          *reinterpret_cast<uint4*>(stage + i * 64 + ((q ^ (i & 15)) << 2)) =
+              make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        if (hf + 1 < D / 64) {
+          load_half(hf + 1, v);
+          if (hf + 2 == D / 64) release_tmem();
+        }
         if (!(ok = group_sync(L::kDQGroup, gq++))) break;  // rows written
         const int cj = lane & 15;  // 16-byte chunk of the row
 #pragma unroll 4
@@ -487,7 +507,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         }
       }
       if (!__all_sync(0xffffffffu, ok)) break;
-      // 3. this warp no longer reads the buffer: the next tile's dS may go in
+      // this warp no longer reads the buffer: the next tile's dS may go in
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kDSFree));
       ++c;
