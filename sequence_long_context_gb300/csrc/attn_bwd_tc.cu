@@ -19,10 +19,13 @@
 //              memory as bf16 (A operands of dV and dK) and dS to shared
 //              memory (A operand of dQ)
 //   warps 8-11 dQ group, one query row per thread: takes the dQ tile out of
-//              tensor memory (freeing it for the next tile), transposes it
-//              through the dS buffer and adds it into the global fp32
-//              accumulator with reductions that each cover whole cache lines
+//              tensor memory (freeing it for the next tile's dP^T),
+//              transposes it through the tile's Q/dO ring slot once the
+//              tile's dV/dK MMAs are done with it, and adds it into the
+//              global fp32 accumulator with reductions that each cover whole
+//              cache lines; then hands the slot to the producer
 //   warp 12    producer: K, V once; then Q, dO tiles through a 2-slot ring
+//              (a slot is refilled after the dQ drain hands it back)
 //   warp 13    MMA issuer and tensor-memory owner
 // Tensor memory (512 columns): S^T [0,128); queries 64g..64g+63 (softmax
 // group g) live in columns [64g, 64g+64) and are overwritten in place by
@@ -64,7 +67,7 @@ struct BSmem {
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
                        kDKVFull = 12, kMmaDone = 13, kGroup = 14, kDQGroup = 15,
-                       kDSFree = 16, kNumBars = 17;
+                       kStageFree = 16, kNumBars = 18;
   // 16-byte aligned: int4 / float4 accesses below
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
@@ -138,7 +141,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kDQFull), 1);
     mbar_init(bar(L::kDQEmpty), kTile / 32);  // one arrival per drain warp
     mbar_init(bar(L::kDQGroup), kTile);
-    mbar_init(bar(L::kDSFree), kTile / 32);
+    for (int s = 0; s < 2; ++s)  // Q/dO slot handed back by the dQ drain
+      mbar_init(bar(L::kStageFree + s), kTile / 32);
     mbar_init(bar(L::kInfoS), 1);
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
@@ -183,7 +187,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           for (int hh = 0; hh < P.G && ok; ++hh) {
             const int h = g * P.G + hh;
             const int slot = n & 1, use = n >> 1;
-            if (use >= 1 && !(ok = mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1,
+            // the slot is free once the dQ drain has used it as staging
+            if (use >= 1 && !(ok = mbar_wait(bar(L::kStageFree + slot), (use - 1) & 1,
                                              abort_flag, P.status)))
               break;
             sched[slot] = make_int4(qt, h, cls, 0);
@@ -200,13 +205,13 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       }
       if (ok) {
         const int slot = n & 1, use = n >> 1;
-        if (use < 1 || mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1, abort_flag,
+        if (use < 1 || mbar_wait(bar(L::kStageFree + slot), (use - 1) & 1, abort_flag,
                                  P.status)) {
           sched[slot] = make_int4(kEnd, 0, 0, 0);
           mbar_arrive(bar(L::kQFull + slot));
         }
         for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
-          if (!mbar_wait(bar(L::kQEmpty + (m & 1)), (m >> 1) & 1, abort_flag, P.status))
+          if (!mbar_wait(bar(L::kStageFree + (m & 1)), (m >> 1) & 1, abort_flag, P.status))
             break;
       }
     }
@@ -365,9 +370,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         tmem_st16(t_s + 64 * half + 16 * cc, pk);  // own columns, already read
       }
       ok = mbar_wait(bar(L::kDPFull), c & 1, abort_flag, P.status);
-      // the dS buffer is still used by the previous tile (its dQ MMAs, then
-      // the dQ drain staging through it)
-      if (ok && c > 0) ok = mbar_wait(bar(L::kDSFree), (c - 1) & 1, abort_flag, P.status);
+      // the dS buffer is still read by the previous tile's dQ MMAs
+      if (ok && c > 0) ok = mbar_wait(bar(L::kDQFull), (c - 1) & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       tmem_wait_st();
@@ -446,7 +450,6 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     const int i = qw * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     int c = 0;
-    int gq = 0;  // uses of the dQ group barrier so far
     // bounded barrier of the 128 drain threads (parity of the use count)
     auto group_sync = [&](int b, int use) -> bool {
       mbar_arrive(bar(b));
@@ -472,44 +475,52 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // Per 64-column half of dQ: rows -> shared memory (the dS buffer, whose
-      // dQ readers have finished), then read back with 16 lanes per 256-byte
-      // row segment so each reduction instruction covers whole cache lines.
-      // 16-byte chunk j of row r lives at chunk j ^ (r & 15). The next half
-      // is taken out of tensor memory while the current one is reduced, and
-      // the columns are released as soon as all of them have been read.
-      float* stage = reinterpret_cast<float*>(sm + L::kDS);
+      // This tile's Q/dO ring slot is free once its dV/dK MMAs are done and
+      // stays free until the producer refills it for two tiles later, far
+      // ahead of need: dQ is staged there (rows of 64 fp32 = 256 bytes,
+      // 16-byte chunk j of row r at chunk j ^ (r & 15)), read back with 16
+      // lanes per row segment so each reduction covers whole cache lines,
+      // and the slot is handed to the producer after the reads.
+      const int slot = c & 1;
+      ok = mbar_wait(bar(L::kQEmpty + slot), (c >> 1) & 1, abort_flag, P.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint8_t* stage_q = sm + L::kQ + slot * L::kTileBytes;
+      uint8_t* stage_do = sm + L::kDO + slot * L::kTileBytes;
+      auto stage_row = [&](int hf, int r) -> float* {
+        if (D == 128) return reinterpret_cast<float*>((hf ? stage_do : stage_q) + r * 256);
+        return reinterpret_cast<float*>((r < 64 ? stage_q : stage_do) + (r & 63) * 256);
+      };
       float* rows_base = P.dq_acc + (((long long)bt * P.S + qt * kTile) * P.Hq + h) * D;
       const long long row_stride = (long long)P.Hq * D;
-      uint32_t v[64];
-      load_half(0, v);
-      if (D == 64) release_tmem();
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
-        if (!(ok = group_sync(L::kDQGroup, gq++))) break;  // buffer free
+        uint32_t v[64];
+        load_half(hf, v);
+        if (hf + 1 == D / 64) release_tmem();
+        float* row = stage_row(hf, i);
 #pragma unroll
         for (int q = 0; q < 16; ++q)
-          *reinterpret_cast<uint4*>(stage + i * 64 + ((q ^ (i & 15)) << 2)) =
+          *reinterpret_cast<uint4*>(row + ((q ^ (i & 15)) << 2)) =
               make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        if (hf + 1 < D / 64) {
-          load_half(hf + 1, v);
-          if (hf + 2 == D / 64) release_tmem();
-        }
-        if (!(ok = group_sync(L::kDQGroup, gq++))) break;  // rows written
-        const int cj = lane & 15;  // 16-byte chunk of the row
+      }
+      if (!(ok = group_sync(L::kDQGroup, c))) break;  // all rows staged
+      const int cj = lane & 15;  // 16-byte chunk of the row
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf) {
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += 2) {
           const int r = qw * 32 + rr + (lane >> 4);
-          const float4 x = *reinterpret_cast<const float4*>(stage + r * 64 +
-                                                           ((cj ^ (r & 15)) << 2));
+          const float4 x =
+              *reinterpret_cast<const float4*>(stage_row(hf, r) + ((cj ^ (r & 15)) << 2));
           red_add_v4(rows_base + r * row_stride + 64 * hf + 4 * cj, x.x * P.scale,
                      x.y * P.scale, x.z * P.scale, x.w * P.scale);
         }
       }
-      if (!__all_sync(0xffffffffu, ok)) break;
-      // this warp no longer reads the buffer: the next tile's dS may go in
+      // the slot's next writer is the producer's TMA (async proxy)
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kDSFree));
+      if (lane == 0) mbar_arrive(bar(L::kStageFree + slot));
       ++c;
     }
   }
