@@ -127,7 +127,6 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   const int kt = ktile_for_rank(P, blockIdx.x / (P.Hkv * P.Bt), ntiles);
   const int g = hb / P.Bt, bt = hb % P.Bt;
   const int kappa = (kt * kTile) / P.shard;  // ring rank owning the key tile
-  const int tiles_per_shard = P.shard / kTile;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kKVFull), 1);
@@ -168,6 +167,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch(&tm_v);
       tma_prefetch(&tm_do);
       const TileSpan ks = tile_span(P, kt * kTile);
+      const PosRange wq = query_window(P, ks);
       mbar_expect_tx(bar(L::kKVFull), 2 * L::kTileBytes);
       for (int hf = 0; hf < L::kHalves; ++hf) {
         tma_load_4d(sbase + L::kK + hf * L::kHalfBytes, &tm_k, bar(L::kKVFull), hf * 64, g,
@@ -180,9 +180,13 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       // the key shard travels the ring: step s finds it on rank kappa + s
       for (int s = 0; s < P.cp && ok; ++s) {
         const int rho = (kappa + s) % P.cp;
-        for (int t = 0; t < tiles_per_shard && ok; ++t) {
-          const int qt = rho * tiles_per_shard + t;
-          const int cls = classify(P, tile_span(P, qt * kTile), ks);
+        // only the runs of the shard that can hold queries seeing the keys
+        TileRun runs[2];
+        const int nr = shard_runs(P, rho, wq, runs);
+        for (int ri = 0; ri < nr && ok; ++ri)
+        for (int qt = runs[ri].begin; qt < runs[ri].end && ok; ++qt) {
+          const TileSpan qsp = tile_span(P, qt * kTile);
+          const int cls = classify(P, qsp, ks);
           if (cls == kClsEmpty) continue;
           for (int hh = 0; hh < P.G && ok; ++hh) {
             const int h = g * P.G + hh;

@@ -102,7 +102,6 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   const int g = h / P.G;
   const int qbase0 = pair * 2 * kBM;          // permuted row of tile 0
   const int rho = qbase0 / P.shard;           // ring rank of both tiles
-  const int tiles_per_shard = P.shard / kBN;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
@@ -136,6 +135,8 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch(&tm_k);
       tma_prefetch(&tm_v);
       const TileSpan q0 = tile_span(P, qbase0), q1 = tile_span(P, qbase0 + kBM);
+      const PosRange w0 = key_window(P, q0), w1 = key_window(P, q1);
+      const PosRange wq = {min(w0.lo, w1.lo), max(w0.hi, w1.hi)};
       mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
       for (int i = 0; i < 2; ++i)
         for (int hf = 0; hf < L::kHalves; ++hf)
@@ -145,10 +146,14 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       bool ok = true;
       for (int s = 0; s < P.cp && ok; ++s) {
         const int kap = (rho - s + P.cp) % P.cp;
-        for (int t = 0; t < tiles_per_shard && ok; ++t) {
-          const int kt = kap * tiles_per_shard + t;
+        // only the runs of the shard that can hold visible keys are visited
+        TileRun runs[2];
+        const int nr = shard_runs(P, kap, wq, runs);
+        for (int ri = 0; ri < nr && ok; ++ri)
+        for (int kt = runs[ri].begin; kt < runs[ri].end && ok; ++kt) {
           const TileSpan ks = tile_span(P, kt * kBN);
-          const int c0 = classify(P, q0, ks), c1 = classify(P, q1, ks);
+          const int c0 = disjoint(ks, w0) ? kEmpty : classify(P, q0, ks);
+          const int c1 = disjoint(ks, w1) ? kEmpty : classify(P, q1, ks);
           if (c0 == kEmpty && c1 == kEmpty) continue;
           const int slot = n & 1, use = n >> 1;
           if (use >= 1 && !(ok = mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1,

@@ -53,6 +53,82 @@ __device__ __forceinline__ int classify(const AttnParams& P, const TileSpan& q,
   return full ? kClsFull : kClsMasked;
 }
 
+// Natural positions [lo, hi] that hold every key some query of tile q can
+// see (a superset): from the start of q's first sequence (or, with a window
+// and no sinks, from q.lo - window + 1) to q.hi (causal) or the end of q's
+// last sequence. Key tiles outside it are empty and are rejected with two
+// comparisons instead of a full classification.
+struct PosRange {
+  int lo, hi;
+};
+__device__ __forceinline__ PosRange key_window(const AttnParams& P, const TileSpan& q) {
+  int s0 = 0, e1 = P.S;
+  if (P.cu != nullptr) {
+    s0 = __ldg(P.cu + seg_of(P.cu, P.nseq, q.lo));
+    e1 = __ldg(P.cu + seg_of(P.cu, P.nseq, q.hi) + 1);
+  }
+  PosRange r;
+  r.lo = (P.window > 0 && P.sink == 0) ? max(s0, q.lo - P.window + 1) : s0;
+  r.hi = P.causal ? q.hi : e1 - 1;
+  return r;
+}
+// Natural positions [lo, hi] that hold every query that can see some key of
+// tile k (a superset), mirroring key_window.
+__device__ __forceinline__ PosRange query_window(const AttnParams& P, const TileSpan& k) {
+  int s0 = 0, e1 = P.S;
+  if (P.cu != nullptr) {
+    s0 = __ldg(P.cu + seg_of(P.cu, P.nseq, k.lo));
+    e1 = __ldg(P.cu + seg_of(P.cu, P.nseq, k.hi) + 1);
+  }
+  PosRange r;
+  r.lo = P.causal ? k.lo : s0;
+  r.hi = (P.window > 0 && P.sink == 0) ? min(e1 - 1, k.hi + P.window - 1) : e1 - 1;
+  return r;
+}
+__device__ __forceinline__ bool disjoint(const TileSpan& t, const PosRange& r) {
+  return t.hi < r.lo || t.lo > r.hi;
+}
+
+__device__ __forceinline__ int floor_div(int a, int b) {  // b > 0
+  return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// Permuted tile indices [begin, end) of ring rank `rank`'s shard whose
+// natural positions can intersect w. A contiguous or stripe shard is one
+// run; a zigzag shard is two chunks, so up to two runs. Returns the count.
+struct TileRun {
+  int begin, end;
+};
+__device__ __forceinline__ int shard_runs(const AttnParams& P, int rank, const PosRange& w,
+                                          TileRun (&runs)[2]) {
+  const int tps = P.shard / kTile;  // tiles per shard
+  const int base = rank * tps;
+  auto clip = [&](int nat0, int ntiles, int tile0, TileRun& r) {
+    // tiles tile0 + t, t in [0, ntiles), hold natural [nat0 + 128 t, +127]
+    int a = max(0, floor_div(w.lo - nat0, kTile));
+    int b = min(ntiles - 1, floor_div(w.hi - nat0, kTile));
+    r.begin = tile0 + a;
+    r.end = tile0 + max(a, b + 1);
+  };
+  if (P.layout == kContiguous) {
+    clip(rank * P.shard, tps, base, runs[0]);
+    return 1;
+  }
+  if (P.layout == kZigzag) {
+    const int cpt = P.chunk / kTile;  // tiles per chunk
+    clip(rank * P.chunk, cpt, base, runs[0]);
+    clip((2 * P.cp - 1 - rank) * P.chunk, cpt, base + cpt, runs[1]);
+    return 2;
+  }
+  // stripe: local tile t holds natural (128 t + i) cp + rank, i in [0, 128)
+  const int span = kTile * P.cp;
+  int a = max(0, -floor_div(-(w.lo - rank - (kTile - 1) * P.cp), span));  // ceil
+  int b = min(tps - 1, floor_div(w.hi - rank, span));
+  runs[0].begin = base + a;
+  runs[0].end = base + max(a, b + 1);
+  return 1;
+}
+
 // Permuted index of the first token of a natural-order run of `len` tokens
 // starting at natural position `pos` (contiguous/zigzag; len divides chunk).
 __device__ __forceinline__ int permuted_of(const AttnParams& P, int pos) {
