@@ -70,9 +70,14 @@ def source_hash(kernel: str):
     src = KERNEL_SOURCES.get(kernel)
     if not src:
         return None
-    path = os.path.join(ROOT, "sequence_long_context_gb300", "csrc", src)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    # the kernel's translation unit and every shared header it may include
+    csrc = os.path.join(ROOT, "sequence_long_context_gb300", "csrc")
+    headers = sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")))
+    h = hashlib.sha256()
+    for name in [src] + headers:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kernel: str, workload: str):
@@ -84,7 +89,7 @@ def traffic_for(kernel: str, workload: str):
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = line.split()
-            if len(parts) == 4 and parts[0] == kernel and parts[1] == workload \
+            if not line.startswith("#") and len(parts) == 4 and parts[0] == kernel and parts[1] == workload \
                     and parts[2] == want:
                 return float(parts[3])
     return None

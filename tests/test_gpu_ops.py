@@ -61,7 +61,7 @@ def _partials(n, rows, D, seed):
     return o, lse
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 7, 8, 17, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 9, 17, 64])
 @pytest.mark.parametrize("tree", [False, True])
 @pytest.mark.parametrize("D", [64, 128])
 def test_merge_matches_oracle(n, tree, D):
