@@ -51,6 +51,9 @@ constexpr int kMmaWarp = 9;
 constexpr int kEmpty = kClsEmpty, kMasked = kClsMasked;
 constexpr int kEnd = -1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Depth of the V ring (the K ring has two slots). A third V slot fits the
+// shared memory but measured no faster.
+constexpr int kVSlots = 2;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
@@ -61,12 +64,13 @@ struct Smem {
   // offsets from the 1024-aligned base
   static constexpr int kQ = 0;                          // 2 query tiles
   static constexpr int kK = kQ + 2 * kTileBytes;        // 2 key slots
-  static constexpr int kV = kK + 2 * kTileBytes;        // 2 value slots
-  static constexpr int kBar = kV + 2 * kTileBytes;
+  static constexpr int kV = kK + 2 * kTileBytes;        // kVSlots value slots
+  static constexpr int kBar = kV + kVSlots * kTileBytes;
   // barriers (8 bytes each)
   static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5,
-                       kVEmpty = 7, kSFull = 9, kPFull = 11, kOFull = 13,
-                       kInfoFull = 15, kMmaDone = 17, kNumBars = 18;
+                       kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots,
+                       kPFull = kSFull + 2, kOFull = kPFull + 2, kInfoFull = kOFull + 2,
+                       kMmaDone = kInfoFull + 2, kNumBars = kMmaDone + 1;
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;             // int2 x 2
   static constexpr int kMisc = kInfo + 16;              // tmem base, abort
@@ -105,11 +109,13 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
+    for (int s = 0; s < kVSlots; ++s) {
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kKEmpty + s), 1);
-      mbar_init(bar(L::kVFull + s), 1);
-      mbar_init(bar(L::kVEmpty + s), 1);
       mbar_init(bar(L::kSFull + s), 1);
       mbar_init(bar(L::kPFull + s), kBM / 32);  // one arrival per softmax warp
       mbar_init(bar(L::kOFull + s), 1);
@@ -142,7 +148,8 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         for (int hf = 0; hf < L::kHalves; ++hf)
           tma_load_4d(sbase + L::kQ + i * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
                       bar(L::kQFull), hf * 64, h, qbase0 + i * kBM, bt);
-      int n = 0;
+      int n = 0;   // key tiles with K and V issued
+      int nk = 0;  // key tiles with K issued (n or n + 1)
       bool ok = true;
       for (int s = 0; s < P.cp && ok; ++s) {
         const int kap = (rho - s + P.cp) % P.cp;
@@ -164,13 +171,15 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           for (int hf = 0; hf < L::kHalves; ++hf)
             tma_load_4d(sbase + L::kK + slot * L::kTileBytes + hf * L::kHalfBytes,
                         &tm_k, bar(L::kKFull + slot), hf * 64, g, kt * kBN, bt);
-          if (use >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + slot), (use - 1) & 1,
-                                           abort_flag, P.status)))
+          ++nk;
+          const int vslot = n % kVSlots, vuse = n / kVSlots;
+          if (vuse >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + vslot), (vuse - 1) & 1,
+                                            abort_flag, P.status)))
             break;
-          mbar_expect_tx(bar(L::kVFull + slot), L::kTileBytes);
+          mbar_expect_tx(bar(L::kVFull + vslot), L::kTileBytes);
           for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_load_4d(sbase + L::kV + slot * L::kTileBytes + hf * L::kHalfBytes,
-                        &tm_v, bar(L::kVFull + slot), hf * 64, g, kt * kBN, bt);
+            tma_load_4d(sbase + L::kV + vslot * L::kTileBytes + hf * L::kHalfBytes,
+                        &tm_v, bar(L::kVFull + vslot), hf * 64, g, kt * kBN, bt);
           ++n;
         }
       }
@@ -182,10 +191,18 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           mbar_arrive(bar(L::kKFull + slot));
         }
         // tail: every issued copy has been consumed before the CTA may exit
-        for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m) {
-          const int sl = m & 1, us = m >> 1;
+        for (int m = (n >= kVSlots ? n - kVSlots : 0); m < n; ++m) {
+          const int sl = m % kVSlots, us = m / kVSlots;
           if (!mbar_wait(bar(L::kVEmpty + sl), us & 1, abort_flag, P.status)) break;
         }
+      }
+      if (*abort_flag) {
+        // aborted: let the copies already issued land before the CTA exits
+        mbar_wait_drain(bar(L::kQFull), 0);
+        for (int m = (nk >= 2 ? nk - 2 : 0); m < nk; ++m)
+          mbar_wait_drain(bar(L::kKFull + (m & 1)), (m >> 1) & 1);
+        for (int m = (n >= kVSlots ? n - kVSlots : 0); m < n; ++m)
+          mbar_wait_drain(bar(L::kVFull + m % kVSlots), (m / kVSlots) & 1);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -213,7 +230,8 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         mma_commit(bar(L::kSFull + i));
         ++cnt[i];
       };
-      // O_i (+)= P_i V(slot); waits for P_i of the latest QK_i and for V.
+      // O_i (+)= P_i V(slot); waits for P_i of the latest QK_i and for V
+      // (slot, use: the V ring's).
       auto pv = [&](int i, int slot, int use, int first) -> bool {
         if (!mbar_wait(bar(L::kPFull + i), (cnt[i] - 1) & 1, abort_flag, P.status))
           return false;
@@ -233,7 +251,8 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       int pend_slot = -1, pend_use = 0, pend_first = 0;  // PV1 still to issue
       int prev_slot = -1;                                // V slot of tile n-1
       while (ok) {
-        const int slot = n & 1, use = n >> 1;
+        const int slot = n & 1, use = n >> 1;            // K slot
+        const int vslot = n % kVSlots, vuse = n / kVSlots;
         if (!(ok = mbar_wait(bar(L::kKFull + slot), use & 1, abort_flag, P.status)))
           break;
         const int4 e = sched[slot];
@@ -257,16 +276,16 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         }
         mma_commit(bar(L::kKEmpty + slot));
         if (e0) {
-          if (!(ok = pv(0, slot, use, first[0]))) break;
+          if (!(ok = pv(0, vslot, vuse, first[0]))) break;
           first[0] = 0;
         }
         if (e1) {
-          pend_slot = slot;
-          pend_use = use;
+          pend_slot = vslot;
+          pend_use = vuse;
           pend_first = first[1];
           first[1] = 0;
         }
-        prev_slot = slot;
+        prev_slot = vslot;
         ++n;
       }
       if (ok && pend_slot >= 0) ok = pv(1, pend_slot, pend_use, pend_first);
@@ -278,7 +297,7 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       }
       // nothing of ours may still run on the tensor core when TMEM is freed
       mma_commit(bar(L::kMmaDone));
-      mbar_wait(bar(L::kMmaDone), 0, abort_flag, P.status);
+      mbar_wait_drain(bar(L::kMmaDone), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -298,6 +317,16 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       const int2 inf = info[i];
       if (inf.x == kEnd) break;
+      // a masked tile: this row's visible keys in the tile (the main
+      // interval and the sink interval of row_visible) as one bit per column
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if (inf.y == kMasked) {
+        const TileSpan ks = tile_span(P, inf.x * kBN);
+        const ColRange c0 = tile_cols(ks, rm.lo, rm.hi);
+        const ColRange c1 = tile_cols(ks, rm.qs, min(rm.sink_end - 1, rm.causal_hi));
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) vis[ch] = col_bits(c0, 32 * ch) | col_bits(c1, 32 * ch);
+      }
       ok = mbar_wait(bar(L::kSFull + i), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -306,11 +335,11 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tm + 32 * ch, sr[ch]);
       tmem_wait_ld();
       if (inf.y == kMasked) {
-        const TileSpan ks = tile_span(P, inf.x * kBN);
 #pragma unroll
-        for (int j = 0; j < 128; ++j)
-          if (!row_visible(rm, ks.lo + j * ks.step))
-            sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
+        for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (!((vis[ch] >> j) & 1u)) sr[ch][j] = __float_as_uint(-INFINITY);
       }
       // row max as 8 independent chains (a single chain is latency-bound)
       float m8[8];

@@ -74,6 +74,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// Waits for a phase like mbar_wait but ignores the abort flag: the clean-up
+// path of an aborted CTA uses it to let its own copies and tensor-core work
+// finish before shared and tensor memory are released. Bounded by the same
+// limit; false if it ran out.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map))

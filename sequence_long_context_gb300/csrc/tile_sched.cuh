@@ -93,6 +93,25 @@ __device__ __forceinline__ int floor_div(int a, int b) {  // b > 0
   return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
+// Columns j of tile t (natural position t.lo + j t.step) whose position lies
+// in [lo, hi], as the range [a, b) (a == b: none).
+struct ColRange {
+  int a, b;
+};
+__device__ __forceinline__ ColRange tile_cols(const TileSpan& t, int lo, int hi) {
+  ColRange r;
+  r.a = min(kTile, max(0, -floor_div(t.lo - lo, t.step)));  // ceil((lo - t.lo) / step)
+  r.b = min(kTile, max(r.a, floor_div(hi - t.lo, t.step) + 1));
+  return r;
+}
+// Bit j (0..31) set when column base + j is in r.
+__device__ __forceinline__ uint32_t col_bits(const ColRange& r, int base) {
+  const int lo = max(r.a - base, 0), hi = min(r.b - base, 32);
+  if (hi <= lo) return 0u;
+  const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+  return below_hi & ~((1u << lo) - 1u);
+}
+
 // Permuted tile indices [begin, end) of ring rank `rank`'s shard whose
 // natural positions can intersect w. A contiguous or stripe shard is one
 // run; a zigzag shard is two chunks, so up to two runs. Returns the count.
