@@ -53,6 +53,22 @@ ProfScope::~ProfScope() {
 
 void note_launch(int n) { g_launches.fetch_add((unsigned long long)n); }
 
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 1;
+  if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 static thread_local char g_detail[256] = "";
 
 usp_status_t fail_cuda_msg(const char* where, const char* msg) {

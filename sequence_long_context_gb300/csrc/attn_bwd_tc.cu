@@ -123,9 +123,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = P.S / kTile;
-  const int hb = blockIdx.x % (P.Hkv * P.Bt);
-  const int kt = ktile_for_rank(P, blockIdx.x / (P.Hkv * P.Bt), ntiles);
-  const int g = hb / P.Bt, bt = hb % P.Bt;
+  const CtaOrder ord = batched_order(blockIdx.x, P.Hkv * P.Bt, ntiles, P.unit_batch);
+  const int kt = ktile_for_rank(P, ord.rank, ntiles);
+  const int g = ord.unit / P.Bt, bt = ord.unit % P.Bt;
   const int kappa = (kt * kTile) / P.shard;  // ring rank owning the key tile
 
   if (threadIdx.x == 0) {
@@ -595,6 +595,12 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   }
   AttnParams Pk = P;
   Pk.status = status;
+  // L2 batches: enough key tiles for about one and a half waves of CTAs
+  {
+    const int ntiles = P.S / kTile;
+    const int per = (3 * sm_count() / 2 + ntiles - 1) / ntiles;
+    Pk.unit_batch = per < P.Hkv * P.Bt ? per : P.Hkv * P.Bt;
+  }
   const int smem = BSmem<D>::kAlloc;
   static bool attr_set = false;
   if (!attr_set) {

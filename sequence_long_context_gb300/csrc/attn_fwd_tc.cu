@@ -81,6 +81,18 @@ struct Smem {
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
 };
 
+// CTA order: units are query heads ordered (kv head, batch, query head of
+// the group), so a batch of consecutive units shares K/V.
+__device__ __forceinline__ CtaOrder fwd_order(const AttnParams& P, int npairs) {
+  return batched_order(blockIdx.x, P.Hq * P.Bt, npairs, P.unit_batch);
+}
+__device__ __forceinline__ int fwd_head(const AttnParams& P, int unit) {
+  return unit / (P.G * P.Bt) * P.G + unit % P.G;
+}
+__device__ __forceinline__ int fwd_batch(const AttnParams& P, int unit) {
+  return (unit / P.G) % P.Bt;
+}
+
 // 10 warps: three share a 16K-register sub-partition, so <= 168 each.
 template <int D>
 __global__ void __maxnreg__(168)
@@ -100,9 +112,9 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int npairs = P.S / (2 * kBM);
-  const int hb = blockIdx.x % (P.Hq * P.Bt);
-  const int pair = qpair_for_rank(P, blockIdx.x / (P.Hq * P.Bt), npairs);
-  const int h = hb / P.Bt, bt = hb % P.Bt;
+  const CtaOrder ord = fwd_order(P, npairs);
+  const int pair = qpair_for_rank(P, ord.rank, npairs);
+  const int h = fwd_head(P, ord.unit), bt = fwd_batch(P, ord.unit);
   const int g = h / P.G;
   const int qbase0 = pair * 2 * kBM;          // permuted row of tile 0
   const int rho = qbase0 / P.shard;           // ring rank of both tiles
@@ -417,6 +429,9 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    // the CTA's head and batch, recomputed (not kept live through the loop)
+    const int unit = fwd_order(P, npairs).unit;
+    const int h = fwd_head(P, unit), bt = fwd_batch(P, unit);
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(P.o) +
                           (((long long)bt * P.S + prow) * P.Hq + h) * D;
 #pragma unroll
@@ -498,6 +513,14 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   }
   AttnParams Pk = P;
   Pk.status = status;
+  // L2 batches: enough query-tile pairs for about two waves of CTAs, in
+  // whole GQA groups
+  {
+    const int npairs = P.S / (2 * kBM);
+    int per = (2 * sm_count() + npairs - 1) / npairs;
+    per = (per + P.G - 1) / P.G * P.G;
+    Pk.unit_batch = per < P.Hq * P.Bt ? per : P.Hq * P.Bt;
+  }
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,

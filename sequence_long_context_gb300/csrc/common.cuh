@@ -50,6 +50,7 @@ struct AttnParams {
   const int* cu;     // varlen boundaries [nseq + 1] or nullptr
   int nseq;
   int cp, layout, shard, chunk;
+  int unit_batch;    // tensor-core kernels: (batch, head) units per L2 batch
 };
 
 __host__ __device__ __forceinline__ int nat_pos(int p, int layout, int cp,

@@ -11,6 +11,9 @@ namespace usp {
 // Counts kernel launches enqueued by this library (usp_launch_count()).
 void note_launch(int n = 1);
 
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
 // Converts the last CUDA error (after a launch) into a status.
 usp_status_t check_launch();
 

@@ -157,6 +157,26 @@ __device__ __forceinline__ int permuted_of(const AttnParams& P, int pos) {
   return (2 * P.cp - 1 - c) * P.shard + C + off;
 }
 
+// Order of the CTAs. The work units (a (batch, head) pair and the tiles of
+// its sequence) are taken in batches of `per` units, sized on the host so a
+// batch has enough CTAs to fill the GPU but keeps few enough heads in flight
+// for their operands (K/V, and in the backward Q/dO and the dQ accumulator)
+// to stay in L2. Inside a batch the CTAs go rank-major (heaviest tiles
+// first, see below), units minor. Returns the unit and the rank of CTA idx.
+struct CtaOrder {
+  int unit, rank;
+};
+__device__ __forceinline__ CtaOrder batched_order(int idx, int nunits, int nranks, int per) {
+  const int batch = idx / (per * nranks);
+  const int u0 = batch * per;
+  const int cnt = min(per, nunits - u0);
+  const int r = idx - batch * per * nranks;
+  CtaOrder o;
+  o.rank = r / cnt;
+  o.unit = u0 + r % cnt;
+  return o;
+}
+
 // Query-tile pairs (256 rows), heaviest first for causal dense problems:
 // later natural positions see more keys.
 __device__ __forceinline__ int qpair_for_rank(const AttnParams& P, int r, int npairs) {
