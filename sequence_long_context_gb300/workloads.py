@@ -76,6 +76,12 @@ WORKLOADS: Dict[str, Workload] = {
         "swa_w1000_sink4_cp8_s8k", B=2, S=8192, Hq=32, Hkv=32, D=128,
         dtype="bf16", causal=True, window=1000, sink_tokens=4, cp=8, ud=1,
         layout="contiguous", backward=False),
+    # the same sliding-window + sink problem as a training step (forward and
+    # backward), the ring sliding-window README's use case (LM training)
+    "swa_w1000_sink4_cp8_s8k_train": Workload(
+        "swa_w1000_sink4_cp8_s8k_train", B=2, S=8192, Hq=32, Hkv=32, D=128,
+        dtype="bf16", causal=True, window=1000, sink_tokens=4, cp=8, ud=1,
+        layout="contiguous", backward=True),
     "varlen_zigzag_cp8_t128k": Workload(
         "varlen_zigzag_cp8_t128k", B=0, S=131072, Hq=32, Hkv=8, D=128,
         dtype="bf16", causal=True, window=0, sink_tokens=0, cp=8, ud=1,

@@ -21,7 +21,8 @@ from tests._gpu import TOL, device, lse_to_natural, rel_fro, run_backward, run_f
 pytestmark = pytest.mark.gpu
 
 CONFIGS = ["usp_ud2_ring4_s8k", "gqa_stripe_cp8_s32k", "swa_w1000_cp8_s8k",
-           "swa_w1000_sink4_cp8_s8k", "varlen_zigzag_cp8_t128k"]
+           "swa_w1000_sink4_cp8_s8k", "swa_w1000_sink4_cp8_s8k_train",
+           "varlen_zigzag_cp8_t128k"]
 
 
 def sample_positions(w, rng, n=40):
