@@ -281,7 +281,10 @@ int usp_profile_read(usp_kernel_stat_t *stats, int max_stats);
  * since the last call: USP_ERR_TIMEOUT if a tensor-core kernel gave up on a
  * pipeline wait (each wait is bounded; a kernel that gives up skips its
  * remaining work, frees its tensor memory and exits, leaving its outputs
- * unspecified), USP_ERR_CUDA if the device reports an error, else USP_OK.
+ * unspecified), USP_ERR_CUDA if the device reports an error or a kernel
+ * found its launch environment unusable (a shared-memory window without the
+ * 1024-byte alignment its swizzled tiles need; it then did nothing), else
+ * USP_OK.
  * Synchronises the whole device: a diagnostics call, not for hot loops. */
 usp_status_t usp_device_status(void);
 

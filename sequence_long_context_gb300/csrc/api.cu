@@ -261,6 +261,7 @@ usp_status_t usp_device_status(void) {
   int a = read_clear_fwd_tc_status(), b = read_clear_bwd_tc_status();
   if (a < 0 || b < 0) return USP_ERR_CUDA;
   if (a == USP_ERR_TIMEOUT || b == USP_ERR_TIMEOUT) return USP_ERR_TIMEOUT;
+  if (a != 0 || b != 0) return USP_ERR_CUDA;
   return USP_OK;
 }
 

@@ -63,19 +63,24 @@ struct BSmem {
   static constexpr int kQ = kV + kTileBytes;        // 2 slots
   static constexpr int kDO = kQ + 2 * kTileBytes;   // 2 slots
   static constexpr int kDS = kDO + 2 * kTileBytes;  // 128 x 128 bf16
-  static constexpr int kBar = kDS + kTile * kTile * 2;
+  // per Q/dO slot: the query tile's LSE*log2e then Delta, 128 fp32 each,
+  // copied in by the producer with the tile
+  static constexpr int kStatBytes = 2 * kTile * 4;
+  static constexpr int kStats = kDS + kTile * kTile * 2;
+  static constexpr int kBar = kStats + 2 * kStatBytes;
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
-                       kDKVFull = 12, kMmaDone = 13, kGroup = 14, kDQGroup = 15,
+                       kDKVFull = 12, kMmaDone = 13, kPReady = 14, kDQGroup = 15,
                        kStageFree = 16, kNumBars = 18;
   // 16-byte aligned: int4 / float4 accesses below
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
   static constexpr int kMisc = kInfo + 32;            // tmem base, abort
-  static constexpr int kRowStats = kMisc + 16;        // LSE*log2e, Delta: 2 x 128 fp32
-  static constexpr int kBytes = kRowStats + 2 * kTile * 4;
-  static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kSched % 16 == 0 && kInfo % 16 == 0 && kRowStats % 16 == 0,
+  static constexpr int kBytes = kMisc + 16;
+  // No alignment slack: the dynamic shared window starts 1024-byte aligned
+  // (checked at kernel entry).
+  static constexpr int kAlloc = kBytes;
+  static_assert(kSched % 16 == 0 && kInfo % 16 == 0 && kStats % 16 == 0,
                 "vector accesses need 16-byte alignment");
   static_assert(kDS % 1024 == 0 && kQ % 1024 == 0 && kDO % 1024 == 0,
                 "128-byte swizzled tiles need 1024-byte alignment");
@@ -111,9 +116,14 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_do) {
   using L = BSmem<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled tiles need a 1024-byte aligned window; there is no slack to
+  // realign into, so a misaligned window is reported and the CTA does nothing
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicExch(P.status, kStatusCudaError);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   const uint32_t sbase = smem_u32(sm);
   auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
   int4* sched = reinterpret_cast<int4*>(sm + L::kSched);
@@ -146,7 +156,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
-    mbar_init(bar(L::kGroup), 2 * kTile);  // all 256 softmax threads
+    mbar_init(bar(L::kPReady), 2 * kTile / 32);  // one arrival per softmax warp
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -196,7 +206,13 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                                              abort_flag, P.status)))
               break;
             sched[slot] = make_int4(qt, h, cls, 0);
-            mbar_expect_tx(bar(L::kQFull + slot), 2 * L::kTileBytes);
+            mbar_expect_tx(bar(L::kQFull + slot), 2 * L::kTileBytes + L::kStatBytes);
+            {
+              const long long row_off = ((long long)bt * P.Hq + h) * P.S + (long long)qt * kTile;
+              const uint32_t st = sbase + L::kStats + slot * L::kStatBytes;
+              bulk_load(st, P.lse2 + row_off, kTile * 4, bar(L::kQFull + slot));
+              bulk_load(st + kTile * 4, P.delta + row_off, kTile * 4, bar(L::kQFull + slot));
+            }
             for (int hf = 0; hf < L::kHalves; ++hf) {
               tma_load_4d(sbase + L::kQ + slot * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
                           bar(L::kQFull + slot), hf * 64, h, qt * kTile, bt);
@@ -223,10 +239,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     // ------------------------------------------------------------ MMA issuer
     // Per query tile n: S^T = K Q^T into [0,128); dP^T = V dO^T into
     // [128,256) once the previous tile's dQ has been taken out of those
-    // columns; when dS is ready: dQ = dS K into [128,256) as one N=D block,
-    // then dV += P^T dO and dK += dS^T Q with P^T / dS^T read as bf16 from
-    // the S^T columns (16 queries per MMA). The next S^T only has
-    // to follow this tile's dV/dK in issue order, never the dQ drain.
+    // columns; when P^T is ready: dV += P^T dO (P^T read as bf16 from the
+    // S^T columns, 16 queries per MMA), overlapping the softmax's dS; when dS
+    // is ready: dQ = dS K into [128,256) as one N=D block, then
+    // dK += dS^T Q. The next S^T only has to follow this tile's dV/dK in
+    // issue order, never the dQ drain.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, 0, 0);
       constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, D, 1, 1);
@@ -267,6 +284,15 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                  kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kDPFull));
+        // dV += P^T dO as soon as P^T is in tensor memory: it runs while the
+        // softmax warps compute dS (K dim = queries; A from tensor memory)
+        if (!(ok = mbar_wait(bar(L::kPReady), n & 1, abort_flag, P.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(t_dv, t_s + 8 * kk + 32 * (kk >> 2),
+                 sdesc_sw128(doa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
+                 (n > 0 || kk > 0) ? 1u : 0u);
         if (!(ok = mbar_wait(bar(L::kDSFull), n & 1, abort_flag, P.status))) break;
         tc_fence_after();
         // dQ = dS K (M = queries, K dim = keys; both operands MN-major)
@@ -275,12 +301,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           mma_ss(t_dp, sdesc_sw128(dsa + kk * 2048, L::kHalfBytes, 1024),
                  sdesc_sw128(ka + kk * 2048, L::kHalfBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
         mma_commit(bar(L::kDQFull));
-        // dV += P^T dO ; dK += dS^T Q  (K dim = queries; A from tensor memory)
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dv, t_s + 8 * kk + 32 * (kk >> 2),
-                 sdesc_sw128(doa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
-                 (n > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(t_dk, t_s + 32 + 8 * kk + 32 * (kk >> 2),
@@ -311,8 +332,6 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
     uint8_t* ds_row = sm + L::kDS + j * 128;
-    float* lse2 = reinterpret_cast<float*>(sm + L::kRowStats);
-    float* delta = lse2 + kTile;
     const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
     int c = 0;
     bool ok = true;
@@ -321,23 +340,15 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       const int4 e = info[0];
       if (e.x == kEnd) break;
-      const int qt = e.x, h = e.y;
+      const int qt = e.x;
       const bool masked = e.z == kClsMasked;
       const TileSpan qs = tile_span(P, qt * kTile);
-      const long long row_off = ((long long)bt * P.Hq + h) * P.S + (long long)qt * kTile;
-      // stage this query tile's LSE (log2 units, loaded by group 0) and Delta
-      // (group 1) in shared memory, overlapping the S^T MMA. A bounded group
-      // barrier of the 256 softmax threads: the previous tile's readers are
-      // done, then the new values are in.
-      const float mine = __ldg((half == 0 ? P.lse2 : P.delta) + row_off + j);
-      mbar_arrive(bar(L::kGroup));
-      ok = mbar_wait(bar(L::kGroup), 0, abort_flag, P.status);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      (half == 0 ? lse2 : delta)[j] = mine;
-      mbar_arrive(bar(L::kGroup));
-      ok = mbar_wait(bar(L::kGroup), 1, abort_flag, P.status);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
+      // this query tile's LSE (log2 units) and Delta, copied into the tile's
+      // Q/dO slot by the producer with the tile itself
+      const float* lse2 = reinterpret_cast<const float*>(sm + L::kStats + (c & 1) * L::kStatBytes);
+      const float* delta = lse2 + kTile;
+      ok = mbar_wait(bar(L::kQFull + (c & 1)), (c >> 1) & 1, abort_flag, P.status);
+      if (ok) ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       // P^T (queries along columns) -> bf16 pairs. Each group writes only
@@ -373,6 +384,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         }
         tmem_st16(t_s + 64 * half + 16 * cc, pk);  // own columns, already read
       }
+      // P^T is in tensor memory: dV may start
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kPReady));
       ok = mbar_wait(bar(L::kDPFull), c & 1, abort_flag, P.status);
       // the dS buffer is still read by the previous tile's dQ MMAs
       if (ok && c > 0) ok = mbar_wait(bar(L::kDQFull), (c - 1) & 1, abort_flag, P.status);

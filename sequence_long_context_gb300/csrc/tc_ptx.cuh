@@ -16,6 +16,7 @@ namespace tc {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kStatusTimeout = 6;                 // USP_ERR_TIMEOUT
+constexpr int kStatusCudaError = 5;               // USP_ERR_CUDA (bad launch environment)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -91,6 +92,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map))
                : "memory");
+}
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global into shared memory; completion is signalled on `bar`
+// as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
 }
 // 4-D tiled load into shared memory; completion is signalled on `bar` as
 // transaction bytes. Coordinates are element indices, innermost first.
