@@ -10,7 +10,7 @@
 // query tile every query head of the GQA group is taken in turn, so dK and
 // dV accumulate in tensor memory over the whole ring and the group and are
 // written once (the shard's ring return). dQ contributions are added into an
-// fp32 accumulator in global memory with vector reductions.
+// fp32 accumulator in global memory by TMA reduce-add operations.
 //
 // Roles (448 threads):
 //   warps 0-7  softmax groups, two threads per key row (each owns 64 of the
@@ -19,11 +19,11 @@
 //              memory as bf16 (A operands of dV and dK) and dS to shared
 //              memory (A operand of dQ)
 //   warps 8-11 dQ group, one query row per thread: takes the dQ tile out of
-//              tensor memory (freeing it for the next tile's dP^T),
-//              transposes it through the tile's Q/dO ring slot once the
-//              tile's dV/dK MMAs are done with it, and adds it into the
-//              global fp32 accumulator with reductions that each cover whole
-//              cache lines; then hands the slot to the producer
+//              tensor memory (freeing it for the next tile's dP^T), stages
+//              it in the tile's Q/dO ring slot once the tile's dV/dK MMAs
+//              are done with it, and has the TMA unit add it into the global
+//              fp32 accumulator; the slot goes back to the producer once the
+//              TMA has read it
 //   warp 12    producer: K, V once; then Q, dO tiles through a 2-slot ring
 //              (a slot is refilled after the dQ drain hands it back)
 //   warp 13    MMA issuer and tensor-memory owner
@@ -71,7 +71,11 @@ struct BSmem {
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
                        kDKVFull = 12, kMmaDone = 13, kPReady = 14, kDQGroup = 15,
-                       kStageFree = 16, kNumBars = 18;
+                       kStageFree = 16, kDOFull = 18, kStageFreeDO = 20, kNumBars = 22;
+  // Each Q/dO slot has two halves with their own full/free barriers: the Q
+  // half (Q tile, LSE and Delta rows; kQFull / kStageFree) and the dO half
+  // (kDOFull / kStageFreeDO). The dQ drain stages through both and frees the
+  // Q half first, so the next tile's Q and S^T need not wait for the rest.
   // 16-byte aligned: int4 / float4 accesses below
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
@@ -114,7 +118,8 @@ __global__ void __maxnreg__(128)
 attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
-                   const __grid_constant__ CUtensorMap tm_do) {
+                   const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_dq) {
   using L = BSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled tiles need a 1024-byte aligned window; there is no slack to
@@ -150,8 +155,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kDQFull), 1);
     mbar_init(bar(L::kDQEmpty), kTile / 32);  // one arrival per drain warp
     mbar_init(bar(L::kDQGroup), kTile);
-    for (int s = 0; s < 2; ++s)  // Q/dO slot handed back by the dQ drain
-      mbar_init(bar(L::kStageFree + s), kTile / 32);
+    for (int s = 0; s < 2; ++s) {  // Q/dO slot halves handed back by the dQ drain
+      mbar_init(bar(L::kStageFree + s), 1);
+      mbar_init(bar(L::kStageFreeDO + s), 1);
+      mbar_init(bar(L::kDOFull + s), 1);
+    }
     mbar_init(bar(L::kInfoS), 1);
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
@@ -185,7 +193,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         tma_load_4d(sbase + L::kV + hf * L::kHalfBytes, &tm_v, bar(L::kKVFull), hf * 64, g,
                     kt * kTile, bt);
       }
-      int n = 0;
+      int n = 0;    // tiles with Q and dO issued
+      int nq = 0;   // tiles with Q issued (n or n + 1)
       bool ok = true;
       // the key shard travels the ring: step s finds it on rank kappa + s
       for (int s = 0; s < P.cp && ok; ++s) {
@@ -201,24 +210,30 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           for (int hh = 0; hh < P.G && ok; ++hh) {
             const int h = g * P.G + hh;
             const int slot = n & 1, use = n >> 1;
-            // the slot is free once the dQ drain has used it as staging
+            // each half of the slot is free once the dQ drain has used it
+            // as staging
             if (use >= 1 && !(ok = mbar_wait(bar(L::kStageFree + slot), (use - 1) & 1,
                                              abort_flag, P.status)))
               break;
             sched[slot] = make_int4(qt, h, cls, 0);
-            mbar_expect_tx(bar(L::kQFull + slot), 2 * L::kTileBytes + L::kStatBytes);
+            mbar_expect_tx(bar(L::kQFull + slot), L::kTileBytes + L::kStatBytes);
             {
               const long long row_off = ((long long)bt * P.Hq + h) * P.S + (long long)qt * kTile;
               const uint32_t st = sbase + L::kStats + slot * L::kStatBytes;
               bulk_load(st, P.lse2 + row_off, kTile * 4, bar(L::kQFull + slot));
               bulk_load(st + kTile * 4, P.delta + row_off, kTile * 4, bar(L::kQFull + slot));
             }
-            for (int hf = 0; hf < L::kHalves; ++hf) {
+            for (int hf = 0; hf < L::kHalves; ++hf)
               tma_load_4d(sbase + L::kQ + slot * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
                           bar(L::kQFull + slot), hf * 64, h, qt * kTile, bt);
+            ++nq;
+            if (use >= 1 && !(ok = mbar_wait(bar(L::kStageFreeDO + slot), (use - 1) & 1,
+                                             abort_flag, P.status)))
+              break;
+            mbar_expect_tx(bar(L::kDOFull + slot), L::kTileBytes);
+            for (int hf = 0; hf < L::kHalves; ++hf)
               tma_load_4d(sbase + L::kDO + slot * L::kTileBytes + hf * L::kHalfBytes, &tm_do,
-                          bar(L::kQFull + slot), hf * 64, h, qt * kTile, bt);
-            }
+                          bar(L::kDOFull + slot), hf * 64, h, qt * kTile, bt);
             ++n;
           }
         }
@@ -231,8 +246,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           mbar_arrive(bar(L::kQFull + slot));
         }
         for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
-          if (!mbar_wait(bar(L::kStageFree + (m & 1)), (m >> 1) & 1, abort_flag, P.status))
+          if (!mbar_wait(bar(L::kStageFree + (m & 1)), (m >> 1) & 1, abort_flag, P.status) ||
+              !mbar_wait(bar(L::kStageFreeDO + (m & 1)), (m >> 1) & 1, abort_flag, P.status))
             break;
+      }
+      if (*abort_flag) {
+        // aborted: let the copies already issued land before the CTA exits
+        mbar_wait_drain(bar(L::kKVFull), 0);
+        for (int m = (nq >= 2 ? nq - 2 : 0); m < nq; ++m)
+          mbar_wait_drain(bar(L::kQFull + (m & 1)), (m >> 1) & 1);
+        for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
+          mbar_wait_drain(bar(L::kDOFull + (m & 1)), (m >> 1) & 1);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -274,6 +298,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         // read its entry) before dP^T and the next drain entry
         if (n > 0 && !(ok = mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status)))
           break;
+        if (!(ok = mbar_wait(bar(L::kDOFull + slot), use & 1, abort_flag, P.status))) break;
         tc_fence_after();
         info[1] = e;
         mbar_arrive(bar(L::kInfoQ));
@@ -319,7 +344,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       info[1] = make_int4(kEnd, n, 0, 0);
       mbar_arrive(bar(L::kInfoQ));
       mma_commit(bar(L::kMmaDone));
-      mbar_wait(bar(L::kMmaDone), 0, abort_flag, P.status);
+      mbar_wait_drain(bar(L::kMmaDone), 0);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
@@ -481,6 +506,15 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_wait_ld();
     };
+    // staging box cg (32 fp32 columns x 128 rows, 16 KB) of a Q/dO slot: the
+    // first D/64 boxes fill the Q tile's space, the rest the dO tile's
+    auto stage_box = [&](int slot, int cg) -> uint8_t* {
+      constexpr int kBoxBytes = kTile * 128;
+      constexpr int kBoxesInQ = L::kTileBytes / kBoxBytes;
+      return cg < kBoxesInQ ? sm + L::kQ + slot * L::kTileBytes + cg * kBoxBytes
+                            : sm + L::kDO + slot * L::kTileBytes + (cg - kBoxesInQ) * kBoxBytes;
+    };
+    const bool leader = qw == 0 && lane == 0;  // issues the reductions
     auto release_tmem = [&]() {  // every dQ column has been read
       tc_fence_before();
       __syncwarp();
@@ -496,53 +530,57 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       // This tile's Q/dO ring slot is free once its dV/dK MMAs are done and
-      // stays free until the producer refills it for two tiles later, far
-      // ahead of need: dQ is staged there (rows of 64 fp32 = 256 bytes,
-      // 16-byte chunk j of row r at chunk j ^ (r & 15)), read back with 16
-      // lanes per row segment so each reduction covers whole cache lines,
-      // and the slot is handed to the producer after the reads.
+      // stays free until the producer refills it for two tiles later: dQ is
+      // staged there, scaled, as D/32 boxes of 32 fp32 columns x 128 rows in
+      // the 128-byte swizzle (16-byte chunk k of row r at k ^ (r & 7)), and
+      // one thread hands the boxes to the TMA unit, which adds them into the
+      // global fp32 accumulator. The slot goes back to the producer as soon
+      // as the TMA has read it; the additions complete asynchronously.
       const int slot = c & 1;
       ok = mbar_wait(bar(L::kQEmpty + slot), (c >> 1) & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint8_t* stage_q = sm + L::kQ + slot * L::kTileBytes;
-      uint8_t* stage_do = sm + L::kDO + slot * L::kTileBytes;
-      auto stage_row = [&](int hf, int r) -> float* {
-        if (D == 128) return reinterpret_cast<float*>((hf ? stage_do : stage_q) + r * 256);
-        return reinterpret_cast<float*>((r < 64 ? stage_q : stage_do) + (r & 63) * 256);
-      };
-      float* rows_base = P.dq_acc + (((long long)bt * P.S + qt * kTile) * P.Hq + h) * D;
-      const long long row_stride = (long long)P.Hq * D;
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
         uint32_t v[64];
         load_half(hf, v);
         if (hf + 1 == D / 64) release_tmem();
-        float* row = stage_row(hf, i);
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          *reinterpret_cast<uint4*>(row + ((q ^ (i & 15)) << 2)) =
-              make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      }
-      if (!(ok = group_sync(L::kDQGroup, c))) break;  // all rows staged
-      const int cj = lane & 15;  // 16-byte chunk of the row
+        for (int cgl = 0; cgl < 2; ++cgl) {
+          uint8_t* rowp = stage_box(slot, 2 * hf + cgl) + i * 128;
 #pragma unroll
-      for (int hf = 0; hf < D / 64; ++hf) {
-#pragma unroll 4
-        for (int rr = 0; rr < 32; rr += 2) {
-          const int r = qw * 32 + rr + (lane >> 4);
-          const float4 x =
-              *reinterpret_cast<const float4*>(stage_row(hf, r) + ((cj ^ (r & 15)) << 2));
-          red_add_v4(rows_base + r * row_stride + 64 * hf + 4 * cj, x.x * P.scale,
-                     x.y * P.scale, x.z * P.scale, x.w * P.scale);
+          for (int k = 0; k < 8; ++k) {
+            const int q = 8 * cgl + k;
+            const float4 x = make_float4(__uint_as_float(v[4 * q]) * P.scale,
+                                         __uint_as_float(v[4 * q + 1]) * P.scale,
+                                         __uint_as_float(v[4 * q + 2]) * P.scale,
+                                         __uint_as_float(v[4 * q + 3]) * P.scale);
+            *reinterpret_cast<float4*>(rowp + ((k ^ (i & 7)) << 4)) = x;
+          }
         }
       }
-      // the slot's next writer is the producer's TMA (async proxy)
+      // the staged rows are read next by the TMA unit (async proxy)
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kStageFree + slot));
+      if (!(ok = group_sync(L::kDQGroup, c))) break;  // all rows staged
+      if (leader) {
+        // the Q half's boxes first, as their own bulk group: that half is
+        // handed back as soon as the TMA has read it
+        constexpr int kBoxesInQ = D / 64;
+#pragma unroll
+        for (int cg = 0; cg < D / 32; ++cg) {
+          tma_reduce_add_4d(&tm_dq, smem_u32(stage_box(slot, cg)), 32 * cg, h, qt * kTile, bt);
+          if (cg + 1 == kBoxesInQ) bulk_commit_group();
+        }
+        bulk_commit_group();
+        bulk_wait_group_read1();
+        mbar_arrive(bar(L::kStageFree + slot));
+        bulk_wait_group_read0();
+        mbar_arrive(bar(L::kStageFreeDO + slot));
+      }
       ++c;
     }
+    // every reduction has landed before the CTA exits
+    if (leader) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -575,18 +613,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
+// [Bt][S][H][D] -> 4-D map (D, H, S, Bt), box (box0, 1, 128, 1), 128B swizzle;
+// bf16 operand tiles (box0 = 64) or the fp32 dQ accumulator (box0 = 32).
+bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
+              bool fp32 = false) {
   auto fn = encode_fn();
   if (!fn) {
     fail_cuda_msg("cuTensorMapEncodeTiled", "driver entry point not found");
     return false;
   }
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)Bt};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
-                           (cuuint64_t)S * H * D * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  const cuuint64_t es_b = fp32 ? 4 : 2;
+  cuuint64_t strides[3] = {(cuuint64_t)D * es_b, (cuuint64_t)H * D * es_b,
+                           (cuuint64_t)S * H * D * es_b};
+  cuuint32_t box[4] = {fp32 ? 32u : 64u, 1, (cuuint32_t)kTile, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims,
                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -600,9 +643,10 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
 
 template <int D>
 usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
-      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D) || !make_map(&mdo, P.dout, P.Bt, P.S, P.Hq, D))
+      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D) || !make_map(&mdo, P.dout, P.Bt, P.S, P.Hq, D) ||
+      !make_map(&mdq, P.dq_acc, P.Bt, P.S, P.Hq, D, true))
     return USP_ERR_CUDA;
   static int* status = nullptr;
   if (status == nullptr) {
@@ -628,7 +672,7 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   const long long blocks = (long long)(P.S / kTile) * P.Hkv * P.Bt;
   {
     ProfScope ps(st, "attn_bwd_tc");
-    attn_bwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv, mdo);
+    attn_bwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv, mdo, mdq);
   }
   note_launch();
   usp_status_t r = check_launch();
