@@ -12,6 +12,8 @@ Modules
              Ulysses sequence<->head all-to-all, as index maps
   merge      the associative log-sum-exp merge of (O, LSE) partials
   ring       a ring simulator: per-chunk partials in ring order + merge
+  decode     a decode step: the newest tokens against a sharded KV cache,
+             and the per-shard partials that a tree merge combines
 
 Every function is pinned by `-m "not gpu"` tests against something other than
 itself (brute force, a library routine, finite differences, closed forms and
