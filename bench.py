@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("causal attn TFLOP/s (useful FLOPs) & % of GB300 BF16 dense peak, "
           "S=8K–128K")
 DEFAULT_WORKLOAD = "usp_ud2_ring4_s8k"
+DEFAULT_DECODE = "decode_gqa_b8_s128k_cp8"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
@@ -41,6 +42,7 @@ KERNEL_SOURCES = {
     "attn_bwd_dkdv_simt": "attn_simt.cu", "attn_bwd_preprocess": "attn_simt.cu",
     "permute_layout": "permute.cu", "permute_ulysses": "permute.cu",
     "merge_linear": "merge.cu", "merge_tree": "merge.cu",
+    "attn_decode_split": "decode.cu",
 }
 
 
@@ -53,6 +55,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -389,6 +392,46 @@ def main():
     except Exception as e:  # report, do not hide
         merge_res = {"error": repr(e)}
 
+    # decode step (split-KV partials over the sharded cache + tree merge) on
+    # its own workload: HBM-bound, reported against the copy bandwidth
+    decode_res = None
+    if not args.no_decode:
+        try:
+            from sequence_long_context_gb300.workloads import (DECODE_WORKLOADS,
+                                                               make_decode_inputs)
+            dw = DECODE_WORKLOADS[DEFAULT_DECODE]
+            dx = make_decode_inputs(dw, seed=args.seed, device=str(dev))
+            dfn = lambda: usp.attn_decode(dx["q"], dx["k"], dx["v"], causal=dw.causal,  # noqa: E731
+                                          cp=dw.cp, splits=dw.splits, tree_order=True)
+            for _ in range(3):
+                dfn()
+            usp.usp_profile_enable(True)
+            dms = timed(dfn, 10)
+            usp.usp_profile_enable(False)
+            dk = usp.usp_profile_read()
+            rows = dw.B * dw.Tq * dw.Hq
+            n_part = dw.cp * dw.splits
+            q_bytes = rows * dw.D * 2
+            part_bytes = n_part * rows * (dw.D + 1) * 4
+            split_bytes = dw.kv_bytes + q_bytes + part_bytes
+            step_bytes = split_bytes + part_bytes + rows * (dw.D * 2 + 4)
+            sp = dk.get("attn_decode_split")
+            split_ms = sp[1] / sp[0] if sp else None
+            decode_res = {
+                "workload": dw.name, "B": dw.B, "Tq": dw.Tq, "S": dw.S, "Hq": dw.Hq,
+                "Hkv": dw.Hkv, "D": dw.D, "cp": dw.cp, "splits": dw.splits,
+                "step_ms": dms, "step_GB_s": step_bytes / (dms * 1e-3) / 1e9,
+                "step_frac_hbm": step_bytes / (dms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                "split_kernel_ms": split_ms,
+                "split_GB_s": split_bytes / (split_ms * 1e-3) / 1e9 if split_ms else None,
+                "split_frac_hbm": (split_bytes / (split_ms * 1e-3) / 1e9 / pk["hbm_gbs"]
+                                   if split_ms else None),
+                "algorithmic_bytes": step_bytes,
+                "traffic": traffic_for("attn_decode_split", dw.name)}
+            del dx
+        except Exception as e:  # report, do not hide
+            decode_res = {"error": repr(e)}
+
     # end to end: pinned host inputs in, results back to pinned host memory
     e2e = None
     if not args.no_e2e:
@@ -434,7 +477,7 @@ def main():
                    "l2": "no flush: step inputs larger than L2"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches * args.steps), "clocks": clocks,
-        "kernels": kernels, "merge": merge_res,
+        "kernels": kernels, "merge": merge_res, "decode": decode_res,
     }
     if rank == 0:
         print(json.dumps(line))

@@ -233,6 +233,44 @@ usp_status_t usp_merge_partials(const float *o_parts, const float *lse_parts,
                                 float *lse_out, usp_stream_t stream);
 
 /*
+ * usp_attn_decode - one decoding step against a KV cache sharded over a ring.
+ *
+ * "Long Context Attention" notes, "Ring Attention": flash decoding is ring
+ * attention at inference time; "Tree Attention": the partials that the
+ * devices compute for a decoding step are combined by a tree reduction
+ * (logsumexp is associative). The newest Tq tokens of every sequence attend
+ * to all S cached keys; token t sits at position S - Tq + t, and with causal
+ * it sees keys j <= S - Tq + t (else all S).
+ *
+ * q    [B, Tq, Hq, D] bf16;  k, v [B, S, Hkv, D] bf16, the cache in rank-major
+ *      contiguous order (rank r's shard is keys [r S/cp, (r+1) S/cp)).
+ * out  [B, Tq, Hq, D] bf16;  lse [B, Tq, Hq] fp32 (natural log of the scaled
+ *      scores' sum).
+ * Every shard is cut into splits_per_shard equal pieces; each piece's partial
+ * (O, LSE) is computed separately (fp32, in the workspace) and the
+ * cp_size * splits_per_shard partials are merged in key order, pairwise
+ * levels (tree_order = 1: a shard's pieces first, then the shards) or left to
+ * right (0), as usp_merge_partials does.
+ * Requirements: Hq % Hkv == 0, (Hq / Hkv) * Tq <= 16, D in {64, 128},
+ * S % (cp_size * splits_per_shard) == 0 and each piece a multiple of 64 keys,
+ * Tq <= S, tree_order: cp_size * splits_per_shard <= 64; 16-byte aligned
+ * pointers; dtype USP_BF16 (USP_FP32 gives USP_ERR_UNSUPPORTED).
+ * workspace: at least usp_attn_decode_workspace_size(...) bytes, 256-byte
+ * aligned; its contents on entry are irrelevant.
+ * Asynchronous on `stream`. Errors: USP_ERR_INVALID_ARG, USP_ERR_UNSUPPORTED,
+ * USP_ERR_ALIGNMENT, USP_ERR_WORKSPACE, USP_ERR_CUDA.
+ */
+usp_status_t usp_attn_decode(const void *q, const void *k, const void *v,
+                             void *out, float *lse, int B, int Tq, int S,
+                             int Hq, int Hkv, int D, float softmax_scale,
+                             int causal, int cp_size, int splits_per_shard,
+                             int tree_order, usp_dtype_t dtype, void *workspace,
+                             size_t workspace_bytes, usp_stream_t stream);
+
+size_t usp_attn_decode_workspace_size(int B, int Tq, int S, int Hq, int Hkv,
+                                      int D, int cp_size, int splits_per_shard);
+
+/*
  * usp_permute - sequence layouts and the Ulysses all-to-all, bit-exact.
  *
  * EXTRACT / RESTORE (the YunChang README's EXTRACT_FUNC_DICT /

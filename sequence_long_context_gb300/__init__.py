@@ -116,6 +116,22 @@ def usp_merge_partials(o_parts, lse_parts, n, rows, D, tree_order, o_out,
         _enum(DTYPE, out_dtype), _p(lse_out), _stream(stream)))
 
 
+def usp_attn_decode(q, k, v, out, lse, B, Tq, S, Hq, Hkv, D, softmax_scale,
+                    causal, cp_size, splits_per_shard, tree_order, dtype,
+                    workspace=None, workspace_bytes=0, stream=None) -> None:
+    _check(_lib.load().usp_attn_decode(
+        _p(q), _p(k), _p(v), _p(out), _p(lse), B, Tq, S, Hq, Hkv, D,
+        float(softmax_scale), int(causal), cp_size, splits_per_shard,
+        int(tree_order), _enum(DTYPE, dtype), _p(workspace),
+        int(workspace_bytes), _stream(stream)))
+
+
+def usp_attn_decode_workspace_size(B, Tq, S, Hq, Hkv, D, cp_size,
+                                   splits_per_shard) -> int:
+    return int(_lib.load().usp_attn_decode_workspace_size(
+        B, Tq, S, Hq, Hkv, D, cp_size, splits_per_shard))
+
+
 def usp_permute(src, dst, kind, layout, B, S, H, D, cp_size, ulysses_degree,
                 elem_bytes, stream=None) -> None:
     _check(_lib.load().usp_permute(
@@ -154,6 +170,21 @@ def _dims(q: torch.Tensor, k: torch.Tensor, cu_seqlens):
         return int(cu_seqlens.numel() - 1), T, Hq, k.shape[1], D, 1
     B, S, Hq, D = q.shape
     return B, S, Hq, k.shape[2], D, B
+
+
+def attn_decode(q, k, v, *, causal=True, cp=1, splits=1, tree_order=True,
+                softmax_scale=0.0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(out [B,Tq,Hq,D], lse [B,Tq,Hq]) of the newest Tq tokens q
+    [B,Tq,Hq,D] against a rank-major contiguous KV cache k, v [B,S,Hkv,D]."""
+    B, Tq, Hq, D = q.shape
+    S, Hkv = k.shape[1], k.shape[2]
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Tq, Hq), dtype=torch.float32, device=q.device)
+    ws_n = usp_attn_decode_workspace_size(B, Tq, S, Hq, Hkv, D, cp, splits)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=q.device)
+    usp_attn_decode(q, k, v, out, lse, B, Tq, S, Hq, Hkv, D, softmax_scale,
+                    causal, cp, splits, tree_order, q.dtype, ws, ws_n, stream)
+    return out, lse
 
 
 def attn_forward(q, k, v, *, causal=True, window=0, sink_tokens=0,

@@ -25,7 +25,7 @@ NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
     "--expt-relaxed-constexpr", "-I", INCLUDE,
 ]
-SOURCES = ["api.cu", "permute.cu", "merge.cu", "attn_simt.cu",
+SOURCES = ["api.cu", "permute.cu", "merge.cu", "attn_simt.cu", "decode.cu",
            "attn_fwd_tc.cu", "attn_bwd_tc.cu", "noalloc.cu"]
 
 

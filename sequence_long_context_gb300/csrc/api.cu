@@ -259,9 +259,11 @@ const char* usp_last_error_detail(void) { return g_detail; }
 usp_status_t usp_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return USP_ERR_CUDA;
   int a = read_clear_fwd_tc_status(), b = read_clear_bwd_tc_status();
-  if (a < 0 || b < 0) return USP_ERR_CUDA;
-  if (a == USP_ERR_TIMEOUT || b == USP_ERR_TIMEOUT) return USP_ERR_TIMEOUT;
-  if (a != 0 || b != 0) return USP_ERR_CUDA;
+  int c = read_clear_decode_status();
+  if (a < 0 || b < 0 || c < 0) return USP_ERR_CUDA;
+  if (a == USP_ERR_TIMEOUT || b == USP_ERR_TIMEOUT || c == USP_ERR_TIMEOUT)
+    return USP_ERR_TIMEOUT;
+  if (a != 0 || b != 0 || c != 0) return USP_ERR_CUDA;
   return USP_OK;
 }
 
@@ -414,6 +416,63 @@ usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
     if ((r = a2a(w.dv, dv, s, Hkv, 0, st)) != USP_OK) return r;
   }
   return USP_OK;
+}
+
+// Decode workspace: the partials [n_part][rows][D] fp32 and [n_part][rows].
+struct DecodeWs {
+  float* o_part;
+  float* lse_part;
+};
+DecodeWs carve_decode(Carve& c, long long rows, int D, int n_part) {
+  DecodeWs w{};
+  w.o_part = static_cast<float*>(c.take((size_t)n_part * rows * D * 4));
+  w.lse_part = static_cast<float*>(c.take((size_t)n_part * rows * 4));
+  return w;
+}
+
+size_t usp_attn_decode_workspace_size(int B, int Tq, int S, int Hq, int Hkv, int D,
+                                      int cp_size, int splits_per_shard) {
+  (void)S;
+  (void)Hkv;
+  if (B < 0 || Tq < 1 || Hq < 1 || D < 1 || cp_size < 1 || splits_per_shard < 1) return 0;
+  Carve c(nullptr);
+  carve_decode(c, (long long)B * Tq * Hq, D, cp_size * splits_per_shard);
+  return c.used;
+}
+
+usp_status_t usp_attn_decode(const void* q, const void* k, const void* v, void* out,
+                             float* lse, int B, int Tq, int S, int Hq, int Hkv, int D,
+                             float softmax_scale, int causal, int cp_size,
+                             int splits_per_shard, int tree_order, usp_dtype_t dtype,
+                             void* workspace, size_t workspace_bytes, usp_stream_t stream) {
+  if (B < 0 || Tq < 1 || S < Tq || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || cp_size < 1 ||
+      splits_per_shard < 1)
+    return USP_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return USP_ERR_INVALID_ARG;
+  if (dtype == USP_FP32) return USP_ERR_UNSUPPORTED;
+  if (dtype != USP_BF16) return USP_ERR_INVALID_ARG;
+  if ((Hq / Hkv) * Tq > decode_max_rows()) return USP_ERR_UNSUPPORTED;
+  const long long n_part = (long long)cp_size * splits_per_shard;
+  if (S % n_part != 0 || (S / n_part) % decode_keys_per_tile() != 0)
+    return USP_ERR_INVALID_ARG;
+  if (tree_order && n_part > 64) return USP_ERR_INVALID_ARG;
+  if (B > 65535 || Hkv > 65535) return USP_ERR_UNSUPPORTED;
+  if (B > 0 && (!q || !k || !v || !out || !lse)) return USP_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, out, lse, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return USP_ERR_ALIGNMENT;
+  if (B == 0) return USP_OK;
+  const long long rows = (long long)B * Tq * Hq;
+  Carve c(workspace);
+  DecodeWs w = carve_decode(c, rows, D, (int)n_part);
+  if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt((float)D);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  usp_status_t r = launch_decode_split(q, k, v, w.o_part, w.lse_part, B, Tq, S, Hq, Hkv, D,
+                                       scale, causal ? 1 : 0, (int)n_part, st);
+  if (r != USP_OK) return r;
+  return launch_merge(w.o_part, w.lse_part, (int)n_part, rows, D, tree_order ? 1 : 0, out, 1,
+                      lse, st);
 }
 
 usp_status_t usp_merge_partials(const float* o_parts, const float* lse_parts,

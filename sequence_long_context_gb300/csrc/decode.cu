@@ -1,0 +1,427 @@
+// Decode-step attention over a sharded KV cache: split-KV partials, then the
+// log-sum-exp merge.
+//
+// "Long Context Attention" notes, "Ring Attention" (flash decoding is ring
+// attention at inference time) and "Tree Attention" (the partials of one
+// decoding step combine by a tree reduction, logsumexp being associative):
+// the newest Tq tokens of each sequence attend to all S cached keys. The
+// cache is in rank-major contiguous order, rank r holding keys
+// [r S/cp, (r+1) S/cp). Every rank's shard is cut into `splits` equal pieces
+// and one CTA computes the partial (O, LSE) of one piece for all the query
+// rows that read one KV head (G query heads x Tq tokens). The standalone
+// merge then combines the pieces in key order (tree order: pairwise levels,
+// so the pieces of one shard meet first, then the shards).
+//
+// HBM-bound: every cached key and value is read once. A CTA streams its piece
+// through shared memory in tiles of 64 keys (TMA, 128-byte swizzle, two
+// stages, three CTAs per SM) and works in three phases per tile:
+//   scores   a lane pair per key, each lane of the pair takes half of D;
+//            q rows are held in shared memory pre-scaled by scale * log2(e)
+//   softmax  a warp per query row: running max m, running sum l, P = 2^(s-m)
+//            written back over the scores, and the rescale factor of O
+//   P V      lanes own output columns; each of the 4 warps folds 16 of the
+//            tile's keys into its own accumulator; they are summed at the end.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace usp {
+namespace {
+
+using namespace tc;
+
+__device__ int g_decode_status = 0;
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int kKeys = 64;     // keys per tile
+constexpr int kMaxRows = 16;  // G * Tq
+constexpr int kStages = 2;    // K/V tiles in flight per CTA (three CTAs fit an SM)
+
+struct DecodeParams {
+  const __nv_bfloat16* q;  // [B][Tq][Hq][D]
+  float* o_part;           // [n_part][B*Tq*Hq][D]
+  float* lse_part;         // [n_part][B*Tq*Hq]
+  int* status;
+  int B, Tq, S, Hq, Hkv, G, R;
+  int n_part, piece;  // pieces and keys per piece
+  float scale_log2;
+  int causal;
+};
+
+// q rows in shared memory: the second half of each row is shifted by 16
+// bytes so that the two lane halves of a warp, which read the same chunk of
+// the two halves, hit different banks (one wavefront instead of two).
+template <int D>
+__host__ __device__ constexpr int kQStride() { return D + 8; }
+template <int D>
+__device__ __forceinline__ int q_index(int r, int d) {
+  return r * kQStride<D>() + d + (d >= D / 2 ? 4 : 0);
+}
+
+template <int D, int R>
+struct DSmem {
+  static constexpr int kTileBytes = kKeys * D * 2;  // one K or V tile
+  static constexpr int kBoxBytes = kKeys * 128;     // 64 columns x 64 keys
+  static constexpr int kK = 0;                      // kStages stages
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kQ = kV + kStages * kTileBytes;  // [R] padded rows, fp32
+  static constexpr int kP = kQ + R * kQStride<D>() * 4;  // [R][64] fp32
+  static constexpr int kStat = kP + R * kKeys * 4;       // m, l, alpha [kMaxRows]
+  static constexpr int kBar = kStat + 3 * kMaxRows * 4;
+  static constexpr int kMisc = kBar + 8 * kStages;      // wait result, abort
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kBar % 8 == 0, "barriers need 8-byte alignment");
+  static_assert(kWarps * R * D * 4 <= 2 * kStages * kTileBytes, "final reduction fits the tiles");
+  static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
+};
+
+template <int D>
+__device__ __forceinline__ const uint8_t* tile_row(const uint8_t* tile, int key, int chunk) {
+  // 16-byte chunk `chunk` (0 .. D/8-1) of key row `key` in a 128-byte swizzled
+  // tile stored as D/64 boxes of 64 keys x 128 bytes
+  const int box = chunk >> 3, c = chunk & 7;
+  return tile + box * (kKeys * 128) + key * 128 + ((c ^ (key & 7)) << 4);
+}
+
+// bf16 pair (one 32-bit word) -> packed fp32 pair (low element first)
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return (static_cast<uint64_t>(w & 0xffff0000u) << 32) | static_cast<uint64_t>(w << 16);
+}
+
+// R: query rows per KV head, padded to a compiled size (rows >= P.R are
+// zero queries whose results are never written).
+template <int D, int R>
+__global__ void __launch_bounds__(kThreads)
+decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v) {
+  using L = DSmem<D, R>;
+  static_assert(R <= kMaxRows, "rows");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
+  float* qs = reinterpret_cast<float*>(sm + L::kQ);
+  float* ps = reinterpret_cast<float*>(sm + L::kP);
+  float* m_run = reinterpret_cast<float*>(sm + L::kStat);
+  float* l_run = m_run + kMaxRows;
+  float* alpha = l_run + kMaxRows;
+  volatile int* wait_ok = reinterpret_cast<volatile int*>(sm + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int piece = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int key0 = piece * P.piece;
+  const int ntiles = P.piece / kKeys;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bar(s), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // query rows r = hh * Tq + t (query head g*G + hh, token t), pre-scaled;
+  // padding rows are zero
+  for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+    const int r = idx / D, d = idx - r * D;
+    float x = 0.f;
+    if (r < P.R) {
+      const int hh = r / P.Tq, t = r - hh * P.Tq;
+      x = __bfloat162float(P.q[(((long long)b * P.Tq + t) * P.Hq + g * P.G + hh) * D + d]) *
+          P.scale_log2;
+    }
+    qs[q_index<D>(r, d)] = x;
+  }
+  if (threadIdx.x < kMaxRows) {
+    m_run[threadIdx.x] = -INFINITY;
+    l_run[threadIdx.x] = 0.f;
+  }
+  __syncthreads();
+
+  auto issue = [&](int i) {  // tile i into stage i % kStages (thread 0)
+    const int st = i % kStages;
+    mbar_expect_tx(bar(st), 2 * L::kTileBytes);
+    for (int hf = 0; hf < D / 64; ++hf) {
+      tma_load_4d(sbase + L::kK + st * L::kTileBytes + hf * L::kBoxBytes, &tm_k, bar(st),
+                  hf * 64, g, key0 + i * kKeys, b);
+      tma_load_4d(sbase + L::kV + st * L::kTileBytes + hf * L::kBoxBytes, &tm_v, bar(st),
+                  hf * 64, g, key0 + i * kKeys, b);
+    }
+  };
+  if (threadIdx.x == 0) {
+    tma_prefetch(&tm_k);
+    tma_prefetch(&tm_v);
+    for (int i = 0; i < kStages && i < ntiles; ++i) issue(i);
+  }
+  int issued = ntiles < kStages ? ntiles : kStages;
+
+  // output accumulators, packed fp32 pairs: lane owns columns
+  // [kCols * lane, kCols * lane + kCols)
+  constexpr int kCols = D / 32, kPairs = kCols / 2;
+  uint64_t o2[R][kPairs];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j) o2[r][j] = 0ull;
+
+  const int qpos0 = P.S - P.Tq;  // position of token t = 0
+  bool ok = true;
+  for (int i = 0; i < ntiles; ++i) {
+    const int st = i % kStages;
+    // one thread waits (bounded) and shares the outcome, so every thread
+    // leaves the loop together
+    if (threadIdx.x == 0)
+      *wait_ok = mbar_wait(bar(st), (i / kStages) & 1, abort_flag, P.status);
+    __syncthreads();
+    if (!*wait_ok) {
+      ok = false;
+      break;
+    }
+    const uint8_t* kt = sm + L::kK + st * L::kTileBytes;
+    const uint8_t* vt = sm + L::kV + st * L::kTileBytes;
+    const int kbase = key0 + i * kKeys;
+
+    // ---- scores: a lane pair per key, each lane half of D
+    {
+      const int kk = warp * 16 + (lane & 15), hs = lane >> 4;
+      uint64_t acc2[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc2[r] = 0ull;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const int chunk = hs * (D / 16) + c;
+        const uint4 raw = *reinterpret_cast<const uint4*>(tile_row<D>(kt, kk, chunk));
+        const uint64_t k0 = bf2_to_f2(raw.x), k1 = bf2_to_f2(raw.y);
+        const uint64_t k2 = bf2_to_f2(raw.z), k3 = bf2_to_f2(raw.w);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float* qp = qs + q_index<D>(r, chunk * 8);
+          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qp);
+          const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qp + 4);
+          acc2[r] = f2_fma(qa.x, k0, acc2[r]);
+          acc2[r] = f2_fma(qa.y, k1, acc2[r]);
+          acc2[r] = f2_fma(qb.x, k2, acc2[r]);
+          acc2[r] = f2_fma(qb.y, k3, acc2[r]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float lo, hi;
+        f2_unpack(acc2[r], lo, hi);
+        float sc = lo + hi;
+        sc += __shfl_xor_sync(0xffffffffu, sc, 16);
+        if (hs == 0) {
+          const int t = r % P.Tq;
+          const bool vis = !P.causal || kbase + kk <= qpos0 + t;
+          ps[r * kKeys + kk] = vis ? sc : -INFINITY;
+        }
+      }
+    }
+    __syncthreads();
+    // ---- softmax: warp per row
+#pragma unroll
+    for (int r0 = 0; r0 < R; r0 += kWarps) {
+      const int r = r0 + warp;
+      if (r < R) {
+        const float s0 = ps[r * kKeys + 2 * lane], s1 = ps[r * kKeys + 2 * lane + 1];
+        float mx = fmaxf(s0, s1);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_old = m_run[r];
+        const float m_new = fmaxf(m_old, mx);
+        float a = 1.f, p0 = 0.f, p1 = 0.f;
+        if (m_new != -INFINITY) {
+          a = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);
+          p0 = (s0 == -INFINITY) ? 0.f : ex2(s0 - m_new);
+          p1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - m_new);
+        }
+        ps[r * kKeys + 2 * lane] = p0;
+        ps[r * kKeys + 2 * lane + 1] = p1;
+        float sum = p0 + p1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        __syncwarp();
+        if (lane == 0) {
+          l_run[r] = l_run[r] * a + sum;
+          m_run[r] = m_new;
+          alpha[r] = a;
+        }
+      }
+    }
+    __syncthreads();
+    // ---- P V: warp folds keys 16 warp .. 16 warp + 15, lane owns columns
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float a = alpha[r];
+      const uint64_t a2 = f2_pack(a, a);
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(o2[r][j], a2, 0ull);
+    }
+    const int col = kCols * lane;
+#pragma unroll 4
+    for (int k16 = 0; k16 < 16; ++k16) {
+      const int key = warp * 16 + k16;
+      // columns col .. col + kCols - 1: chunk col / 8, byte offset within it
+      const uint8_t* src = tile_row<D>(vt, key, col >> 3) + (col & 7) * 2;
+      uint64_t v2[kPairs];
+      if constexpr (kPairs == 2) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src);
+        v2[0] = bf2_to_f2(raw.x);
+        v2[1] = bf2_to_f2(raw.y);
+      } else {
+        v2[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(src));
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float p = ps[r * kKeys + key];
+        const uint64_t p2 = f2_pack(p, p);
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(p2, v2[j], o2[r][j]);
+      }
+    }
+    __syncthreads();  // stage st and the P buffer are free again
+    if (i + kStages < ntiles) {
+      if (threadIdx.x == 0) issue(i + kStages);
+      issued = i + kStages + 1;
+    }
+  }
+  if (!ok) {
+    // aborted: let the copies already issued (the latest one of each stage)
+    // land before the CTA exits
+    if (threadIdx.x == 0)
+      for (int i = (issued >= kStages ? issued - kStages : 0); i < issued; ++i)
+        mbar_wait_drain(bar(i % kStages), (i / kStages) & 1);
+    return;
+  }
+  // ---- the warps' accumulators, summed through the (now idle) tiles
+  float* red = reinterpret_cast<float*>(sm + L::kK);  // [kWarps][R][D]
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j)
+      *reinterpret_cast<uint64_t*>(red + (warp * R + r) * D + kCols * lane + 2 * j) = o2[r][j];
+  __syncthreads();
+  const long long rows = (long long)P.B * P.Tq * P.Hq;
+  for (int idx = threadIdx.x; idx < P.R * D; idx += kThreads) {
+    const int r = idx / D, d = idx - r * D;
+    const int hh = r / P.Tq, t = r - hh * P.Tq;
+    const long long row = ((long long)b * P.Tq + t) * P.Hq + g * P.G + hh;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) sum += red[(w * R + r) * D + d];
+    const float l = l_run[r];
+    P.o_part[((long long)piece * rows + row) * D + d] = l > 0.f ? sum / l : 0.f;
+    if (d == 0)
+      P.lse_part[(long long)piece * rows + row] =
+          l > 0.f ? (m_run[r] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [B][S][Hkv][D] bf16 cache -> 4-D map (D, Hkv, S, B), box (64, 1, 64, 1).
+bool make_cache_map(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
+  auto fn = encode_fn();
+  if (!fn) {
+    fail_cuda_msg("cuTensorMapEncodeTiled", "driver entry point not found");
+    return false;
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                           (cuuint64_t)S * H * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kKeys, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    std::snprintf(msg, sizeof(msg), "CUresult %d", (int)r);
+    fail_cuda_msg("cuTensorMapEncodeTiled", msg);
+    return false;
+  }
+  return true;
+}
+
+template <int D>
+usp_status_t launch_d(const DecodeParams& P, const void* k, const void* v, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  if (!make_cache_map(&mk, k, P.B, P.S, P.Hkv, D) || !make_cache_map(&mv, v, P.B, P.S, P.Hkv, D))
+    return USP_ERR_CUDA;
+  static int* status = nullptr;
+  if (status == nullptr) {
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_decode_status);
+    if (e != cudaSuccess) return fail_cuda("cudaGetSymbolAddress(status)", e);
+  }
+  DecodeParams Pk = P;
+  Pk.status = status;
+  dim3 grid(P.n_part, P.Hkv, P.B);
+  auto go = [&](auto kernel, int smem) -> usp_status_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem);
+    if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(smem)", e);
+    {
+      ProfScope ps(st, "attn_decode_split");
+      kernel<<<grid, kThreads, smem, st>>>(Pk, mk, mv);
+    }
+    note_launch();
+    return check_launch();
+  };
+  if (P.R <= 1) return go(decode_split_kernel<D, 1>, DSmem<D, 1>::kAlloc);
+  if (P.R <= 2) return go(decode_split_kernel<D, 2>, DSmem<D, 2>::kAlloc);
+  if (P.R <= 4) return go(decode_split_kernel<D, 4>, DSmem<D, 4>::kAlloc);
+  if (P.R <= 8) return go(decode_split_kernel<D, 8>, DSmem<D, 8>::kAlloc);
+  return go(decode_split_kernel<D, 16>, DSmem<D, 16>::kAlloc);
+}
+
+}  // namespace
+
+int read_clear_decode_status() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) cudaMemcpyToSymbol(g_decode_status, &z, sizeof(int));
+  return v;
+}
+
+int decode_max_rows() { return kMaxRows; }
+int decode_keys_per_tile() { return kKeys; }
+
+usp_status_t launch_decode_split(const void* q, const void* k, const void* v, float* o_part,
+                                 float* lse_part, int B, int Tq, int S, int Hq, int Hkv, int D,
+                                 float scale, int causal, int n_part, cudaStream_t st) {
+  DecodeParams P{};
+  P.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  P.o_part = o_part;
+  P.lse_part = lse_part;
+  P.B = B;
+  P.Tq = Tq;
+  P.S = S;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.G = Hq / Hkv;
+  P.R = P.G * Tq;
+  P.n_part = n_part;
+  P.piece = S / n_part;
+  P.scale_log2 = scale * 1.4426950408889634f;
+  P.causal = causal;
+  return D == 128 ? launch_d<128>(P, k, v, st) : launch_d<64>(P, k, v, st);
+}
+
+}  // namespace usp

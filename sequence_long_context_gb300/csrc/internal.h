@@ -59,6 +59,13 @@ usp_status_t launch_fwd_tc(const AttnParams& P, cudaStream_t st);
 int read_clear_fwd_tc_status();  // -1 on a CUDA error
 
 // attn_bwd_tc.cu (tcgen05 tensor-core backward, bf16)
+usp_status_t launch_decode_split(const void* q, const void* k, const void* v, float* o_part,
+                                 float* lse_part, int B, int Tq, int S, int Hq, int Hkv, int D,
+                                 float scale, int causal, int n_part, cudaStream_t st);
+int read_clear_decode_status();  // -1 on a CUDA error
+int decode_max_rows();
+int decode_keys_per_tile();
+
 bool bwd_tc_supported(const AttnParams& P);
 usp_status_t launch_bwd_tc(const AttnParams& P, cudaStream_t st);
 int read_clear_bwd_tc_status();  // -1 on a CUDA error

@@ -153,3 +153,53 @@ def n_segments(w: Workload, inputs: Dict[str, torch.Tensor]) -> int:
     if w.varlen:
         return int(inputs["cu_seqlens"].numel() - 1)
     return w.B
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One decoding step: the newest Tq tokens against a KV cache of S keys
+    sharded over cp ranks (rank-major contiguous), each shard cut into
+    `splits` pieces whose partials are merged in tree order."""
+    name: str
+    B: int
+    Tq: int
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    cp: int
+    splits: int
+    causal: bool = True
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def kv_bytes(self) -> int:
+        return 2 * self.B * self.S * self.Hkv * self.D * 2
+
+
+# The pages give no decode shape; this one reuses the GQA sweep's heads
+# (32 query / 8 KV heads, D = 128) and its longest sequence as the cache,
+# sharded over the same 8-way ring, one new token for 8 sequences.
+DECODE_WORKLOADS: Dict[str, DecodeWorkload] = {
+    "decode_gqa_b8_s128k_cp8": DecodeWorkload(
+        "decode_gqa_b8_s128k_cp8", B=8, Tq=1, S=131072, Hq=32, Hkv=8, D=128,
+        cp=8, splits=4),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload, seed: int = 0, device: str = "cpu"
+                       ) -> Dict[str, torch.Tensor]:
+    """Seeded bf16 q [B,Tq,Hq,D] and cache k, v [B,S,Hkv,D] (N(0,1) drawn in
+    fp32, then rounded)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+
+    def rnd(shape):
+        return torch.randn(shape, generator=g, device=device,
+                           dtype=torch.float32).to(torch.bfloat16)
+
+    return {"q": rnd((w.B, w.Tq, w.Hq, w.D)),
+            "k": rnd((w.B, w.S, w.Hkv, w.D)),
+            "v": rnd((w.B, w.S, w.Hkv, w.D))}

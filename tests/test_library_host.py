@@ -103,3 +103,38 @@ def test_empty_problem_is_a_no_op(lib):
 def test_python_binding_raises(lib):
     with pytest.raises(usp.UspError, match="USP_ERR_INVALID_ARG"):
         usp._check(1)
+
+
+def decode(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, B=2, Tq=1, S=1024, Hq=8,
+             Hkv=2, D=128, scale=0.0, causal=1, cp=4, splits=2, tree=1, dtype=0,
+             ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(over)
+    return lib.usp_attn_decode(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"],
+                               a["Tq"], a["S"], a["Hq"], a["Hkv"], a["D"], a["scale"],
+                               a["causal"], a["cp"], a["splits"], a["tree"], a["dtype"],
+                               a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Hq=7), 1),                  # Hq % Hkv
+    (dict(Tq=5), 2),                  # G * Tq = 20 rows > 16
+    (dict(S=1000), 1),                # S % (cp * splits)
+    (dict(S=256), 1),                 # pieces of 32 keys, not a multiple of 64
+    (dict(D=96), 1),
+    (dict(dtype=1), 2),               # fp32 cache: unsupported
+    (dict(cp=16, splits=8, S=8192), 1),  # tree order over more than 64 partials
+    (dict(q=FAKE + 4), 3),
+    (dict(ws=None), 4),               # no workspace
+    (dict(wsb=16), 4),                # workspace too small
+    (dict(Tq=2000), 1),               # more new tokens than cached keys
+])
+def test_decode_rejects_before_launch(lib, over, code):
+    assert decode(lib, **over) == code
+
+
+def test_decode_workspace_and_empty_batch(lib):
+    n = usp.usp_attn_decode_workspace_size(2, 1, 1024, 8, 2, 128, 4, 2)
+    rows = 2 * 1 * 8
+    assert n >= 8 * rows * 128 * 4 + 8 * rows * 4
+    assert decode(lib, B=0, q=None, k=None, v=None, out=None, lse=None) == 0
