@@ -70,7 +70,8 @@ struct Smem {
   static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5,
                        kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots,
                        kPFull = kSFull + 2, kOFull = kPFull + 2, kInfoFull = kOFull + 2,
-                       kMmaDone = kInfoFull + 2, kNumBars = kMmaDone + 1;
+                       kMmaDone = kInfoFull + 2, kOStaged = kMmaDone + 1,
+                       kNumBars = kOStaged + 2;
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;             // int2 x 2
   static constexpr int kMisc = kInfo + 16;              // tmem base, abort
@@ -98,7 +99,8 @@ template <int D>
 __global__ void __maxnreg__(168)
 attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v) {
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_o) {
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -132,6 +134,7 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       mbar_init(bar(L::kPFull + s), kBM / 32);  // one arrival per softmax warp
       mbar_init(bar(L::kOFull + s), 1);
       mbar_init(bar(L::kInfoFull + s), 1);
+      mbar_init(bar(L::kOStaged + s), kBM / 32);  // one arrival per softmax warp
     }
     mbar_init(bar(L::kMmaDone), 1);
     *abort_flag = 0;
@@ -424,35 +427,56 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) mbar_arrive(bar(L::kPFull + i));  // one arrival per warp
       ++c;
     }
-    // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2
+    // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2. The rows are
+    // staged in the 128-byte swizzle in this query tile's shared-memory slot
+    // (free: every Q K^T has completed when O is) and one thread of the
+    // group stores the tile with TMA.
     if (ok) ok = mbar_wait(bar(L::kOFull + i), 0, abort_flag, P.status);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
     // the CTA's head and batch, recomputed (not kept live through the loop)
     const int unit = fwd_order(P, npairs).unit;
     const int h = fwd_head(P, unit), bt = fwd_batch(P, unit);
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(P.o) +
-                          (((long long)bt * P.S + prow) * P.Hq + h) * D;
+    if (ok) {
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      uint8_t* stage = sm + L::kQ + i * L::kTileBytes;
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t o[32];
-      tmem_ld32(o_tm + 32 * ch, o);
-      tmem_wait_ld();
-      uint4 w[4];
-      uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(o_tm + 32 * ch, o);
+        tmem_wait_ld();
+        uint32_t wp[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float a = (c > 0) ? __uint_as_float(o[2 * j]) * inv : 0.f;
-        const float b = (c > 0) ? __uint_as_float(o[2 * j + 1]) * inv : 0.f;
-        wp[j] = pack_bf16(a, b);
+        for (int j = 0; j < 16; ++j) {
+          const float a = (c > 0) ? __uint_as_float(o[2 * j]) * inv : 0.f;
+          const float b = (c > 0) ? __uint_as_float(o[2 * j + 1]) * inv : 0.f;
+          wp[j] = pack_bf16(a, b);
+        }
+        // columns 32 ch .. 32 ch + 31 = 16-byte chunks 4 ch .. 4 ch + 3 of
+        // the row, in 64-column halves
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c8 = 4 * ch + q, hf = c8 >> 3, chunk = c8 & 7;
+          *reinterpret_cast<uint4*>(stage + hf * L::kHalfBytes + r * 128 +
+                                    ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(wp[4 * q], wp[4 * q + 1], wp[4 * q + 2], wp[4 * q + 3]);
+        }
       }
-      uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) dst[j] = w[j];
+      fence_proxy_async_smem();  // the staged rows are read next by the TMA unit
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kOStaged + i));
+      if (quarter == 0 && lane == 0) {
+        if (mbar_wait(bar(L::kOStaged + i), 0, abort_flag, P.status)) {
+          for (int hf = 0; hf < L::kHalves; ++hf)
+            tma_store_4d(&tm_o, smem_u32(stage + hf * L::kHalfBytes), hf * 64, h,
+                         qbase0 + i * kBM, bt);
+          bulk_commit_group();
+          bulk_wait_group0();  // the tile has left shared memory before the CTA exits
+        }
+      }
+      P.lse[lse_index(P, bt, h, prow)] =
+          (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     }
-    P.lse[lse_index(P, bt, h, prow)] =
-        (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
   }
 
   tc_fence_before();
@@ -501,9 +525,9 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
 
 template <int D>
 usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
-      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D))
+      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D) || !make_map(&mo, P.o, P.Bt, P.S, P.Hq, D))
     return USP_ERR_CUDA;  // detail recorded by make_map
   const int smem = Smem<D>::kAlloc;
   static int* status = nullptr;
@@ -531,7 +555,7 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   const long long blocks = (long long)(P.S / (2 * kBM)) * P.Hq * P.Bt;
   {
     ProfScope ps(st, "attn_fwd_tc");
-    attn_fwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv);
+    attn_fwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv, mo);
   }
   note_launch();
   return check_launch();
