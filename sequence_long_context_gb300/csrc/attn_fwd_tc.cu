@@ -156,8 +156,9 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch(&tm_k);
       tma_prefetch(&tm_v);
       const TileSpan q0 = tile_span(P, qbase0), q1 = tile_span(P, qbase0 + kBM);
-      const PosRange w0 = key_window(P, q0), w1 = key_window(P, q1);
-      const PosRange wq = {min(w0.lo, w1.lo), max(w0.hi, w1.hi)};
+      const KeyWindows w0 = key_windows(P, q0), w1 = key_windows(P, q1);
+      const PosRange band = {min(w0.band.lo, w1.band.lo), max(w0.band.hi, w1.band.hi)};
+      const PosRange sinks = {min(w0.sink.lo, w1.sink.lo), max(w0.sink.hi, w1.sink.hi)};
       mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
       for (int i = 0; i < 2; ++i)
         for (int hf = 0; hf < L::kHalves; ++hf)
@@ -166,37 +167,50 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       int n = 0;   // key tiles with K and V issued
       int nk = 0;  // key tiles with K issued (n or n + 1)
       bool ok = true;
+      // one key tile: classified for both query tiles, loaded unless empty
+      // for both
+      auto visit = [&](int kt) {
+        const TileSpan ks = tile_span(P, kt * kBN);
+        const int c0 = (disjoint(ks, w0.band) && disjoint(ks, w0.sink)) ? kEmpty
+                                                                      : classify(P, q0, ks);
+        const int c1 = (disjoint(ks, w1.band) && disjoint(ks, w1.sink)) ? kEmpty
+                                                                      : classify(P, q1, ks);
+        if (c0 == kEmpty && c1 == kEmpty) return;
+        const int slot = n & 1, use = n >> 1;
+        if (use >= 1 && !(ok = mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1,
+                                         abort_flag, P.status)))
+          return;
+        sched[slot] = make_int4(kt, c0, c1, 0);
+        mbar_expect_tx(bar(L::kKFull + slot), L::kTileBytes);
+        for (int hf = 0; hf < L::kHalves; ++hf)
+          tma_load_4d(sbase + L::kK + slot * L::kTileBytes + hf * L::kHalfBytes,
+                      &tm_k, bar(L::kKFull + slot), hf * 64, g, kt * kBN, bt);
+        ++nk;
+        const int vslot = n % kVSlots, vuse = n / kVSlots;
+        if (vuse >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + vslot), (vuse - 1) & 1,
+                                          abort_flag, P.status)))
+          return;
+        mbar_expect_tx(bar(L::kVFull + vslot), L::kTileBytes);
+        for (int hf = 0; hf < L::kHalves; ++hf)
+          tma_load_4d(sbase + L::kV + vslot * L::kTileBytes + hf * L::kHalfBytes,
+                      &tm_v, bar(L::kVFull + vslot), hf * 64, g, kt * kBN, bt);
+        ++n;
+      };
       for (int s = 0; s < P.cp && ok; ++s) {
         const int kap = (rho - s + P.cp) % P.cp;
-        // only the runs of the shard that can hold visible keys are visited
-        TileRun runs[2];
-        const int nr = shard_runs(P, kap, wq, runs);
-        for (int ri = 0; ri < nr && ok; ++ri)
-        for (int kt = runs[ri].begin; kt < runs[ri].end && ok; ++kt) {
-          const TileSpan ks = tile_span(P, kt * kBN);
-          const int c0 = disjoint(ks, w0) ? kEmpty : classify(P, q0, ks);
-          const int c1 = disjoint(ks, w1) ? kEmpty : classify(P, q1, ks);
-          if (c0 == kEmpty && c1 == kEmpty) continue;
-          const int slot = n & 1, use = n >> 1;
-          if (use >= 1 && !(ok = mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1,
-                                           abort_flag, P.status)))
-            break;
-          sched[slot] = make_int4(kt, c0, c1, 0);
-          mbar_expect_tx(bar(L::kKFull + slot), L::kTileBytes);
-          for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_load_4d(sbase + L::kK + slot * L::kTileBytes + hf * L::kHalfBytes,
-                        &tm_k, bar(L::kKFull + slot), hf * 64, g, kt * kBN, bt);
-          ++nk;
-          const int vslot = n % kVSlots, vuse = n / kVSlots;
-          if (vuse >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + vslot), (vuse - 1) & 1,
-                                            abort_flag, P.status)))
-            break;
-          mbar_expect_tx(bar(L::kVFull + vslot), L::kTileBytes);
-          for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_load_4d(sbase + L::kV + vslot * L::kTileBytes + hf * L::kHalfBytes,
-                        &tm_v, bar(L::kVFull + vslot), hf * 64, g, kt * kBN, bt);
-          ++n;
-        }
+        // only the runs of the shard that can hold visible keys are visited:
+        // the sink tokens' tiles first, then the band's (without those)
+        TileRun sr[2], br[2];
+        const int nsr = sinks.lo <= sinks.hi ? shard_runs(P, kap, sinks, sr) : 0;
+        const int nbr = shard_runs(P, kap, band, br);
+        for (int ri = 0; ri < nsr && ok; ++ri)
+          for (int kt = sr[ri].begin; kt < sr[ri].end && ok; ++kt) visit(kt);
+        for (int ri = 0; ri < nbr && ok; ++ri)
+          for (int kt = br[ri].begin; kt < br[ri].end && ok; ++kt) {
+            bool seen = false;
+            for (int rj = 0; rj < nsr; ++rj) seen |= kt >= sr[rj].begin && kt < sr[rj].end;
+            if (!seen) visit(kt);
+          }
       }
       if (ok) {
         const int slot = n & 1, use = n >> 1;

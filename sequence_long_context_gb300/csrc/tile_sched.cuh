@@ -53,40 +53,61 @@ __device__ __forceinline__ int classify(const AttnParams& P, const TileSpan& q,
   return full ? kClsFull : kClsMasked;
 }
 
-// Natural positions [lo, hi] that hold every key some query of tile q can
-// see (a superset): from the start of q's first sequence (or, with a window
-// and no sinks, from q.lo - window + 1) to q.hi (causal) or the end of q's
-// last sequence. Key tiles outside it are empty and are rejected with two
-// comparisons instead of a full classification.
 struct PosRange {
-  int lo, hi;
+  int lo, hi;  // natural positions lo .. hi; empty when lo > hi
 };
-__device__ __forceinline__ PosRange key_window(const AttnParams& P, const TileSpan& q) {
-  int s0 = 0, e1 = P.S;
+
+// Natural positions that can hold keys visible to some query of tile q (a
+// superset), in two ranges: the band, from the start of q's first sequence
+// (with a window: from q.lo - window + 1) to q.hi (causal) or the end of q's
+// last sequence; and, with a window and attention sinks, the sink tokens of
+// q's sequences (else empty). Key tiles outside both are empty and are
+// rejected with a few comparisons instead of a full classification.
+struct KeyWindows {
+  PosRange band, sink;
+};
+__device__ __forceinline__ KeyWindows key_windows(const AttnParams& P, const TileSpan& q) {
+  int s0 = 0, s1 = 0, e1 = P.S;
   if (P.cu != nullptr) {
+    const int n1 = seg_of(P.cu, P.nseq, q.hi);
     s0 = __ldg(P.cu + seg_of(P.cu, P.nseq, q.lo));
-    e1 = __ldg(P.cu + seg_of(P.cu, P.nseq, q.hi) + 1);
+    s1 = __ldg(P.cu + n1);
+    e1 = __ldg(P.cu + n1 + 1);
   }
-  PosRange r;
-  r.lo = (P.window > 0 && P.sink == 0) ? max(s0, q.lo - P.window + 1) : s0;
-  r.hi = P.causal ? q.hi : e1 - 1;
-  return r;
+  KeyWindows w;
+  w.band.lo = P.window > 0 ? max(s0, q.lo - P.window + 1) : s0;
+  w.band.hi = P.causal ? q.hi : e1 - 1;
+  if (P.window > 0 && P.sink > 0) {
+    w.sink.lo = s0;
+    w.sink.hi = s1 + P.sink - 1;
+  } else {
+    w.sink.lo = 1;
+    w.sink.hi = 0;
+  }
+  return w;
 }
-// Natural positions [lo, hi] that hold every query that can see some key of
-// tile k (a superset), mirroring key_window.
+// Natural positions [lo, hi] that can hold queries seeing some key of tile k
+// (a superset): from k.lo (causal) or the start of k's first sequence to the
+// end of k's last sequence, or, with a window, to k.hi + window - 1 unless
+// the tile may hold sink tokens (seen by every later query of their
+// sequence).
 __device__ __forceinline__ PosRange query_window(const AttnParams& P, const TileSpan& k) {
   int s0 = 0, e1 = P.S;
+  bool multi = false;
   if (P.cu != nullptr) {
-    s0 = __ldg(P.cu + seg_of(P.cu, P.nseq, k.lo));
-    e1 = __ldg(P.cu + seg_of(P.cu, P.nseq, k.hi) + 1);
+    const int n0 = seg_of(P.cu, P.nseq, k.lo), n1 = seg_of(P.cu, P.nseq, k.hi);
+    s0 = __ldg(P.cu + n0);
+    e1 = __ldg(P.cu + n1 + 1);
+    multi = n0 != n1;
   }
+  const bool sinks = P.sink > 0 && (multi || k.lo < s0 + P.sink);
   PosRange r;
   r.lo = P.causal ? k.lo : s0;
-  r.hi = (P.window > 0 && P.sink == 0) ? min(e1 - 1, k.hi + P.window - 1) : e1 - 1;
+  r.hi = (P.window > 0 && !sinks) ? min(e1 - 1, k.hi + P.window - 1) : e1 - 1;
   return r;
 }
 __device__ __forceinline__ bool disjoint(const TileSpan& t, const PosRange& r) {
-  return t.hi < r.lo || t.lo > r.hi;
+  return r.lo > r.hi || t.hi < r.lo || t.lo > r.hi;
 }
 
 __device__ __forceinline__ int floor_div(int a, int b) {  // b > 0
