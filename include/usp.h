@@ -326,6 +326,20 @@ int usp_profile_read(usp_kernel_stat_t *stats, int max_stats);
  * Synchronises the whole device: a diagnostics call, not for hot loops. */
 usp_status_t usp_device_status(void);
 
+/*
+ * usp_selftest_wait_timeout - exercise the failure path of usp_device_status.
+ *
+ * A diagnostics call with no counterpart on the pages. It launches one small
+ * kernel whose pipeline wait (the same bounded mbarrier wait the attention
+ * kernels use) waits on a phase that nothing ever completes. After limit_us
+ * microseconds (1 .. 1000000) the wait gives up, records USP_ERR_TIMEOUT in
+ * a device status word and the kernel exits normally: the next
+ * usp_device_status() then returns USP_ERR_TIMEOUT (and clears it), and the
+ * device stays usable. Nothing faults or traps. Asynchronous on `stream`.
+ * Errors: USP_ERR_INVALID_ARG (limit out of range), USP_ERR_CUDA.
+ */
+usp_status_t usp_selftest_wait_timeout(unsigned limit_us, usp_stream_t stream);
+
 /* Which CUDA call failed, and why, for the last USP_ERR_CUDA returned on the
  * calling thread (thread-local storage, never NULL; empty if none). */
 const char *usp_last_error_detail(void);

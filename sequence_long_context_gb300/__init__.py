@@ -148,6 +148,12 @@ def usp_device_status() -> None:
     _check(_lib.load().usp_device_status())
 
 
+def usp_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch a kernel whose bounded wait must time out after limit_us
+    (diagnostics: the next usp_device_status() reports USP_ERR_TIMEOUT)."""
+    _check(_lib.load().usp_selftest_wait_timeout(int(limit_us), _stream(stream)))
+
+
 def usp_profile_enable(on: bool) -> None:
     _check(_lib.load().usp_profile_enable(int(bool(on))))
 

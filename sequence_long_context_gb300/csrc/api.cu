@@ -259,12 +259,18 @@ const char* usp_last_error_detail(void) { return g_detail; }
 usp_status_t usp_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return USP_ERR_CUDA;
   int a = read_clear_fwd_tc_status(), b = read_clear_bwd_tc_status();
-  int c = read_clear_decode_status();
-  if (a < 0 || b < 0 || c < 0) return USP_ERR_CUDA;
-  if (a == USP_ERR_TIMEOUT || b == USP_ERR_TIMEOUT || c == USP_ERR_TIMEOUT)
+  int c = read_clear_decode_status(), d = read_clear_selftest_status();
+  if (a < 0 || b < 0 || c < 0 || d < 0) return USP_ERR_CUDA;
+  if (a == USP_ERR_TIMEOUT || b == USP_ERR_TIMEOUT || c == USP_ERR_TIMEOUT ||
+      d == USP_ERR_TIMEOUT)
     return USP_ERR_TIMEOUT;
-  if (a != 0 || b != 0 || c != 0) return USP_ERR_CUDA;
+  if (a != 0 || b != 0 || c != 0 || d != 0) return USP_ERR_CUDA;
   return USP_OK;
+}
+
+usp_status_t usp_selftest_wait_timeout(unsigned limit_us, usp_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return USP_ERR_INVALID_ARG;
+  return launch_selftest_wait_timeout(limit_us, reinterpret_cast<cudaStream_t>(stream));
 }
 
 usp_status_t usp_profile_enable(int on) {

@@ -63,6 +63,8 @@ usp_status_t launch_decode_split(const void* q, const void* k, const void* v, fl
                                  float* lse_part, int B, int Tq, int S, int Hq, int Hkv, int D,
                                  float scale, int causal, int n_part, cudaStream_t st);
 int read_clear_decode_status();  // -1 on a CUDA error
+usp_status_t launch_selftest_wait_timeout(unsigned limit_us, cudaStream_t st);
+int read_clear_selftest_status();  // -1 on a CUDA error
 int decode_max_rows();
 int decode_keys_per_tile();
 

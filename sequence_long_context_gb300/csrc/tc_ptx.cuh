@@ -57,17 +57,18 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Waits for the phase of `bar` with the given parity to complete. Returns
-// false if it did not within kWaitLimitNs (recording USP_ERR_TIMEOUT in
-// *status and raising the CTA's abort flag) or once *abort is raised.
+// false if it did not within limit_ns (recording USP_ERR_TIMEOUT in *status
+// and raising the CTA's abort flag) or once *abort is raised.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort, int* status) {
+                                          volatile int* abort, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) break;
+      if (global_ns() - t0 > limit_ns) break;
     }
   }
   *abort = 1;

@@ -138,3 +138,8 @@ def test_decode_workspace_and_empty_batch(lib):
     rows = 2 * 1 * 8
     assert n >= 8 * rows * 128 * 4 + 8 * rows * 4
     assert decode(lib, B=0, q=None, k=None, v=None, out=None, lse=None) == 0
+
+
+def test_selftest_rejects_limits(lib):
+    assert lib.usp_selftest_wait_timeout(0, None) == 1
+    assert lib.usp_selftest_wait_timeout(2_000_000, None) == 1
