@@ -14,13 +14,15 @@
 //
 // HBM-bound: every cached key and value is read once. A CTA streams its piece
 // through shared memory in tiles of 64 keys (TMA, 128-byte swizzle, two
-// stages, three CTAs per SM) and works in three phases per tile:
+// stages filled by a producer warp, three CTAs per SM). Each of the four
+// compute warps takes 16 keys of every tile and runs its own online softmax
+// over them, so no block-wide barrier is needed inside the loop:
 //   scores   a lane pair per key, each lane of the pair takes half of D;
 //            q rows are held in shared memory pre-scaled by scale * log2(e)
-//   softmax  a warp per query row: running max m, running sum l, P = 2^(s-m)
-//            written back over the scores, and the rescale factor of O
-//   P V      lanes own output columns; each of the 4 warps folds 16 of the
-//            tile's keys into its own accumulator; they are summed at the end.
+//   softmax  running max m and sum l per query row by warp shuffles,
+//            P = 2^(s - m) to a warp-private buffer, O rescaled
+//   P V      lanes own output columns
+// At the end the four warps' (m, l, O) are merged with the log-sum-exp rule.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -35,8 +37,8 @@ using namespace tc;
 
 __device__ int g_decode_status = 0;
 
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
+constexpr int kComputeWarps = 4;
+constexpr int kThreads = 32 * (kComputeWarps + 1);  // + one producer warp
 constexpr int kKeys = 64;     // keys per tile
 constexpr int kMaxRows = 16;  // G * Tq
 constexpr int kStages = 2;    // K/V tiles in flight per CTA (three CTAs fit an SM)
@@ -69,14 +71,15 @@ struct DSmem {
   static constexpr int kK = 0;                      // kStages stages
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kQ = kV + kStages * kTileBytes;  // [R] padded rows, fp32
-  static constexpr int kP = kQ + R * kQStride<D>() * 4;  // [R][64] fp32
-  static constexpr int kStat = kP + R * kKeys * 4;       // m, l, alpha [kMaxRows]
-  static constexpr int kBar = kStat + 3 * kMaxRows * 4;
-  static constexpr int kMisc = kBar + 8 * kStages;      // wait result, abort
+  static constexpr int kP = kQ + R * kQStride<D>() * 4;  // per warp [R][16] fp32
+  static constexpr int kMerge = kP + kComputeWarps * R * 16 * 4;  // per warp m, l [R]
+  static constexpr int kBar = kMerge + 2 * kComputeWarps * kMaxRows * 4;
+  static constexpr int kMisc = kBar + 8 * 2 * kStages;  // abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kBar % 8 == 0, "barriers need 8-byte alignment");
-  static_assert(kWarps * R * D * 4 <= 2 * kStages * kTileBytes, "final reduction fits the tiles");
+  static_assert(kComputeWarps * R * D * 4 <= 2 * kStages * kTileBytes,
+                "the final merge fits the tiles");
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
 };
 
@@ -105,14 +108,10 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
-  auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
+  auto full = [&](int s) { return sbase + L::kBar + 8 * s; };
+  auto empty = [&](int s) { return sbase + L::kBar + 8 * (kStages + s); };
   float* qs = reinterpret_cast<float*>(sm + L::kQ);
-  float* ps = reinterpret_cast<float*>(sm + L::kP);
-  float* m_run = reinterpret_cast<float*>(sm + L::kStat);
-  float* l_run = m_run + kMaxRows;
-  float* alpha = l_run + kMaxRows;
-  volatile int* wait_ok = reinterpret_cast<volatile int*>(sm + L::kMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int piece = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -120,7 +119,10 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
   const int ntiles = P.piece / kKeys;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(bar(s), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kComputeWarps);  // one arrival per compute warp
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -136,58 +138,63 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
     }
     qs[q_index<D>(r, d)] = x;
   }
-  if (threadIdx.x < kMaxRows) {
-    m_run[threadIdx.x] = -INFINITY;
-    l_run[threadIdx.x] = 0.f;
-  }
   __syncthreads();
 
-  auto issue = [&](int i) {  // tile i into stage i % kStages (thread 0)
-    const int st = i % kStages;
-    mbar_expect_tx(bar(st), 2 * L::kTileBytes);
-    for (int hf = 0; hf < D / 64; ++hf) {
-      tma_load_4d(sbase + L::kK + st * L::kTileBytes + hf * L::kBoxBytes, &tm_k, bar(st),
-                  hf * 64, g, key0 + i * kKeys, b);
-      tma_load_4d(sbase + L::kV + st * L::kTileBytes + hf * L::kBoxBytes, &tm_v, bar(st),
-                  hf * 64, g, key0 + i * kKeys, b);
-    }
-  };
-  if (threadIdx.x == 0) {
-    tma_prefetch(&tm_k);
-    tma_prefetch(&tm_v);
-    for (int i = 0; i < kStages && i < ntiles; ++i) issue(i);
-  }
-  int issued = ntiles < kStages ? ntiles : kStages;
-
-  // output accumulators, packed fp32 pairs: lane owns columns
-  // [kCols * lane, kCols * lane + kCols)
   constexpr int kCols = D / 32, kPairs = kCols / 2;
-  uint64_t o2[R][kPairs];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int j = 0; j < kPairs; ++j) o2[r][j] = 0ull;
-
-  const int qpos0 = P.S - P.Tq;  // position of token t = 0
-  bool ok = true;
-  for (int i = 0; i < ntiles; ++i) {
-    const int st = i % kStages;
-    // one thread waits (bounded) and shares the outcome, so every thread
-    // leaves the loop together
-    if (threadIdx.x == 0)
-      *wait_ok = mbar_wait(bar(st), (i / kStages) & 1, abort_flag, P.status);
-    __syncthreads();
-    if (!*wait_ok) {
-      ok = false;
-      break;
+  if (warp == kComputeWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch(&tm_k);
+      tma_prefetch(&tm_v);
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
+        // the stage is free once every compute warp has released tile i - kStages
+        if (i >= kStages &&
+            !mbar_wait(empty(st), (i / kStages - 1) & 1, abort_flag, P.status))
+          break;
+        mbar_expect_tx(full(st), 2 * L::kTileBytes);
+        for (int hf = 0; hf < D / 64; ++hf) {
+          tma_load_4d(sbase + L::kK + st * L::kTileBytes + hf * L::kBoxBytes, &tm_k, full(st),
+                      hf * 64, g, key0 + i * kKeys, b);
+          tma_load_4d(sbase + L::kV + st * L::kTileBytes + hf * L::kBoxBytes, &tm_v, full(st),
+                      hf * 64, g, key0 + i * kKeys, b);
+        }
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        // aborted: let the copies already issued land before the tiles are reused
+        for (int i = (issued >= kStages ? issued - kStages : 0); i < issued; ++i)
+          mbar_wait_drain(full(i % kStages), (i / kStages) & 1);
+      }
     }
-    const uint8_t* kt = sm + L::kK + st * L::kTileBytes;
-    const uint8_t* vt = sm + L::kV + st * L::kTileBytes;
-    const int kbase = key0 + i * kKeys;
-
-    // ---- scores: a lane pair per key, each lane half of D
-    {
-      const int kk = warp * 16 + (lane & 15), hs = lane >> 4;
+  } else {
+    // ---------------------------------------------------------- compute warps
+    // Each warp runs its own online softmax over its 16 keys of every tile:
+    // running max m, running sum l and the O accumulator (packed fp32 pairs,
+    // lane owns columns kCols*lane ..), merged across warps at the end.
+    float* pw = reinterpret_cast<float*>(sm + L::kP) + warp * R * 16;  // [R][16]
+    float m[R], l[R];
+    uint64_t o2[R][kPairs];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      m[r] = -INFINITY;
+      l[r] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) o2[r][j] = 0ull;
+    }
+    const int qpos0 = P.S - P.Tq;  // position of token t = 0
+    const int kk = warp * 16 + (lane & 15), hs = lane >> 4;
+    const int col = kCols * lane;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % kStages;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(full(st), (i / kStages) & 1, abort_flag, P.status);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const uint8_t* kt = sm + L::kK + st * L::kTileBytes;
+      const uint8_t* vt = sm + L::kV + st * L::kTileBytes;
+      const int kpos = key0 + i * kKeys + kk;
+      // scores: a lane pair per key, each lane half of D
       uint64_t acc2[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) acc2[r] = 0ull;
@@ -208,117 +215,109 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
           acc2[r] = f2_fma(qb.y, k3, acc2[r]);
         }
       }
+      // softmax over the warp's 16 keys (both lane halves hold the same
+      // values after the first reduction; later ones stay within a half)
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         float lo, hi;
         f2_unpack(acc2[r], lo, hi);
         float sc = lo + hi;
         sc += __shfl_xor_sync(0xffffffffu, sc, 16);
-        if (hs == 0) {
-          const int t = r % P.Tq;
-          const bool vis = !P.causal || kbase + kk <= qpos0 + t;
-          ps[r * kKeys + kk] = vis ? sc : -INFINITY;
-        }
-      }
-    }
-    __syncthreads();
-    // ---- softmax: warp per row
+        if (P.causal && kpos > qpos0 + r % P.Tq) sc = -INFINITY;
+        float mx = sc;
 #pragma unroll
-    for (int r0 = 0; r0 < R; r0 += kWarps) {
-      const int r = r0 + warp;
-      if (r < R) {
-        const float s0 = ps[r * kKeys + 2 * lane], s1 = ps[r * kKeys + 2 * lane + 1];
-        float mx = fmaxf(s0, s1);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float m_old = m_run[r];
-        const float m_new = fmaxf(m_old, mx);
-        float a = 1.f, p0 = 0.f, p1 = 0.f;
+        for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m[r], mx);
+        float a = 1.f, p = 0.f;
         if (m_new != -INFINITY) {
-          a = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);
-          p0 = (s0 == -INFINITY) ? 0.f : ex2(s0 - m_new);
-          p1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - m_new);
+          a = (m[r] == -INFINITY) ? 0.f : ex2(m[r] - m_new);
+          p = (sc == -INFINITY) ? 0.f : ex2(sc - m_new);
         }
-        ps[r * kKeys + 2 * lane] = p0;
-        ps[r * kKeys + 2 * lane + 1] = p1;
-        float sum = p0 + p1;
+        float sum = p;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        __syncwarp();
-        if (lane == 0) {
-          l_run[r] = l_run[r] * a + sum;
-          m_run[r] = m_new;
-          alpha[r] = a;
-        }
+        for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        l[r] = l[r] * a + sum;
+        m[r] = m_new;
+        const uint64_t a2 = f2_pack(a, a);
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(o2[r][j], a2, 0ull);
+        if (hs == 0) pw[r * 16 + (lane & 15)] = p;
       }
-    }
-    __syncthreads();
-    // ---- P V: warp folds keys 16 warp .. 16 warp + 15, lane owns columns
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float a = alpha[r];
-      const uint64_t a2 = f2_pack(a, a);
-#pragma unroll
-      for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(o2[r][j], a2, 0ull);
-    }
-    const int col = kCols * lane;
+      __syncwarp();
+      // P V over the warp's 16 keys, lane owns columns
 #pragma unroll 4
-    for (int k16 = 0; k16 < 16; ++k16) {
-      const int key = warp * 16 + k16;
-      // columns col .. col + kCols - 1: chunk col / 8, byte offset within it
-      const uint8_t* src = tile_row<D>(vt, key, col >> 3) + (col & 7) * 2;
-      uint64_t v2[kPairs];
-      if constexpr (kPairs == 2) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(src);
-        v2[0] = bf2_to_f2(raw.x);
-        v2[1] = bf2_to_f2(raw.y);
-      } else {
-        v2[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(src));
+      for (int k16 = 0; k16 < 16; ++k16) {
+        const int key = warp * 16 + k16;
+        const uint8_t* src = tile_row<D>(vt, key, col >> 3) + (col & 7) * 2;
+        uint64_t v2[kPairs];
+        if constexpr (kPairs == 2) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(src);
+          v2[0] = bf2_to_f2(raw.x);
+          v2[1] = bf2_to_f2(raw.y);
+        } else {
+          v2[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(src));
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float pp = pw[r * 16 + k16];
+          const uint64_t p2 = f2_pack(pp, pp);
+#pragma unroll
+          for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(p2, v2[j], o2[r][j]);
+        }
       }
+      __syncwarp();  // this warp is done with the stage and with its P buffer
+      if (lane == 0) mbar_arrive(empty(st));
+    }
+    // every compute warp is done with the tiles (named barrier of the four
+    // compute warps, reached on the abort path too) before the partials
+    // overwrite them
+    asm volatile("bar.sync 1, %0;" ::"r"(kComputeWarps * 32) : "memory");
+    // this warp's partial: m, l per row and its O columns (through the
+    // now idle tiles)
+    float* mw = reinterpret_cast<float*>(sm + L::kMerge);
+    float* lw = mw + kComputeWarps * kMaxRows;
+    float* red = reinterpret_cast<float*>(sm + L::kK);  // [warps][R][D]
+    if (lane == 0) {
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float p = ps[r * kKeys + key];
-        const uint64_t p2 = f2_pack(p, p);
-#pragma unroll
-        for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(p2, v2[j], o2[r][j]);
+        mw[warp * kMaxRows + r] = m[r];
+        lw[warp * kMaxRows + r] = l[r];
       }
     }
-    __syncthreads();  // stage st and the P buffer are free again
-    if (i + kStages < ntiles) {
-      if (threadIdx.x == 0) issue(i + kStages);
-      issued = i + kStages + 1;
-    }
-  }
-  if (!ok) {
-    // aborted: let the copies already issued (the latest one of each stage)
-    // land before the CTA exits
-    if (threadIdx.x == 0)
-      for (int i = (issued >= kStages ? issued - kStages : 0); i < issued; ++i)
-        mbar_wait_drain(bar(i % kStages), (i / kStages) & 1);
-    return;
-  }
-  // ---- the warps' accumulators, summed through the (now idle) tiles
-  float* red = reinterpret_cast<float*>(sm + L::kK);  // [kWarps][R][D]
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int j = 0; j < kPairs; ++j)
-      *reinterpret_cast<uint64_t*>(red + (warp * R + r) * D + kCols * lane + 2 * j) = o2[r][j];
+      for (int j = 0; j < kPairs; ++j)
+        *reinterpret_cast<uint64_t*>(red + (warp * R + r) * D + col + 2 * j) = o2[r][j];
+  }
   __syncthreads();
+  if (*abort_flag) return;
+  // merge the warps' partials with the log-sum-exp rule (log2 units)
+  const float* mw = reinterpret_cast<const float*>(sm + L::kMerge);
+  const float* lw = mw + kComputeWarps * kMaxRows;
+  const float* red = reinterpret_cast<const float*>(sm + L::kK);
   const long long rows = (long long)P.B * P.Tq * P.Hq;
   for (int idx = threadIdx.x; idx < P.R * D; idx += kThreads) {
     const int r = idx / D, d = idx - r * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, mw[w * kMaxRows + r]);
+    float Ls = 0.f, Os = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) {
+        const float mwr = mw[w * kMaxRows + r];
+        const float f = (mwr == -INFINITY) ? 0.f : ex2(mwr - M);
+        Ls += lw[w * kMaxRows + r] * f;
+        Os += red[(w * R + r) * D + d] * f;
+      }
+    }
     const int hh = r / P.Tq, t = r - hh * P.Tq;
     const long long row = ((long long)b * P.Tq + t) * P.Hq + g * P.G + hh;
-    float sum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) sum += red[(w * R + r) * D + d];
-    const float l = l_run[r];
-    P.o_part[((long long)piece * rows + row) * D + d] = l > 0.f ? sum / l : 0.f;
+    P.o_part[((long long)piece * rows + row) * D + d] = Ls > 0.f ? Os / Ls : 0.f;
     if (d == 0)
       P.lse_part[(long long)piece * rows + row] =
-          l > 0.f ? (m_run[r] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          Ls > 0.f ? (M + log2f(Ls)) * 0.6931471805599453f : -INFINITY;
   }
 }
 
