@@ -71,7 +71,8 @@ struct BSmem {
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
                        kDKVFull = 12, kMmaDone = 13, kPReady = 14, kDQGroup = 15,
-                       kStageFree = 16, kDOFull = 18, kStageFreeDO = 20, kNumBars = 22;
+                       kStageFree = 16, kDOFull = 18, kStageFreeDO = 20, kKVStaged = 22,
+                       kNumBars = 24;
   // Each Q/dO slot has two halves with their own full/free barriers: the Q
   // half (Q tile, LSE and Delta rows; kQFull / kStageFree) and the dO half
   // (kDOFull / kStageFreeDO). The dQ drain stages through both and frees the
@@ -119,7 +120,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_do,
-                   const __grid_constant__ CUtensorMap tm_dq) {
+                   const __grid_constant__ CUtensorMap tm_dq,
+                   const __grid_constant__ CUtensorMap tm_dk,
+                   const __grid_constant__ CUtensorMap tm_dv) {
   using L = BSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled tiles need a 1024-byte aligned window; there is no slack to
@@ -165,6 +168,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kDKVFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
     mbar_init(bar(L::kPReady), 2 * kTile / 32);  // one arrival per softmax warp
+    for (int s = 0; s < 2; ++s) mbar_init(bar(L::kKVStaged + s), kTile / 32);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -464,30 +468,48 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) mbar_arrive(bar(L::kDSFull));
       ++c;
     }
-    // epilogue: group 0 writes dV, group 1 writes scale * dK for its key row
+    // epilogue: group 0 writes dV, group 1 writes scale * dK for its key
+    // row, staged in the 128-byte swizzle in the V / K tile (free: every MMA
+    // has completed) and stored with TMA by one thread of the group
     if (ok) ok = mbar_wait(bar(L::kDKVFull), 0, abort_flag, P.status);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    const long long off = (((long long)bt * P.S + kp) * P.Hkv + g) * D;
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(half ? P.dk : P.dv) + off;
-    const uint32_t src = tmem + lane_off + 256 + half * D;
-    const float mul = half ? P.scale : 1.f;
+    if (ok) {
+      uint8_t* stage = sm + (half ? L::kK : L::kV);
+      const uint32_t src = tmem + lane_off + 256 + half * D;
+      const float mul = half ? P.scale : 1.f;
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t o[32];
-      tmem_ld32(src + 32 * ch, o);
-      tmem_wait_ld();
-      uint4 w[4];
-      uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(src + 32 * ch, o);
+        tmem_wait_ld();
+        uint32_t wp[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float a = c > 0 ? __uint_as_float(o[2 * k]) * mul : 0.f;
-        const float b = c > 0 ? __uint_as_float(o[2 * k + 1]) * mul : 0.f;
-        wp[k] = pack_bf16(a, b);
+        for (int k = 0; k < 16; ++k) {
+          const float a = c > 0 ? __uint_as_float(o[2 * k]) * mul : 0.f;
+          const float b = c > 0 ? __uint_as_float(o[2 * k + 1]) * mul : 0.f;
+          wp[k] = pack_bf16(a, b);
+        }
+        // columns 32 ch .. 32 ch + 31 = 16-byte chunks 4 ch .. 4 ch + 3
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c8 = 4 * ch + q, hf = c8 >> 3, chunk = c8 & 7;
+          *reinterpret_cast<uint4*>(stage + hf * L::kHalfBytes + j * 128 +
+                                    ((chunk ^ (j & 7)) << 4)) =
+              make_uint4(wp[4 * q], wp[4 * q + 1], wp[4 * q + 2], wp[4 * q + 3]);
+        }
       }
-      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * ch);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) d4[k] = w[k];
+      fence_proxy_async_smem();  // read next by the TMA unit
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kKVStaged + half));
+      if (quarter == 0 && lane == 0 &&
+          mbar_wait(bar(L::kKVStaged + half), 0, abort_flag, P.status)) {
+        for (int hf = 0; hf < L::kHalves; ++hf)
+          tma_store_4d(half ? &tm_dk : &tm_dv, smem_u32(stage + hf * L::kHalfBytes), hf * 64,
+                       g, kt * kTile, bt);
+        bulk_commit_group();
+        bulk_wait_group0();  // the tile has left shared memory before the CTA exits
+      }
     }
   } else {
     // ------------------------------------------------------------ dQ drain
@@ -643,10 +665,11 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
 
 template <int D>
 usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
       !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D) || !make_map(&mdo, P.dout, P.Bt, P.S, P.Hq, D) ||
-      !make_map(&mdq, P.dq_acc, P.Bt, P.S, P.Hq, D, true))
+      !make_map(&mdq, P.dq_acc, P.Bt, P.S, P.Hq, D, true) ||
+      !make_map(&mdk, P.dk, P.Bt, P.S, P.Hkv, D) || !make_map(&mdv, P.dv, P.Bt, P.S, P.Hkv, D))
     return USP_ERR_CUDA;
   static int* status = nullptr;
   if (status == nullptr) {
@@ -672,7 +695,7 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   const long long blocks = (long long)(P.S / kTile) * P.Hkv * P.Bt;
   {
     ProfScope ps(st, "attn_bwd_tc");
-    attn_bwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv, mdo, mdq);
+    attn_bwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv, mdo, mdq, mdk, mdv);
   }
   note_launch();
   usp_status_t r = check_launch();
