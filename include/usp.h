@@ -233,6 +233,41 @@ usp_status_t usp_merge_partials(const float *o_parts, const float *lse_parts,
                                 float *lse_out, usp_stream_t stream);
 
 /*
+ * usp_attn_fwd_qkvpacked / usp_attn_bwd_qkvpacked - the same calls on one
+ * packed tensor.
+ *
+ * The YunChang README's LongContextAttentionQKVPacked ("2. Usage"; its
+ * benchmark conclusions find the packed form faster) takes q, k and v as one
+ * tensor. qkv [B, S, 3, H, D] (rank-major order, as usp_permute(EXTRACT)
+ * gives when called with 3*H heads), Hq = Hkv = H: q is qkv[:, :, 0], k
+ * qkv[:, :, 1], v qkv[:, :, 2]. Nothing is unpacked: the kernels read the
+ * three parts in place with a token stride of 3*H*D elements (and the
+ * Ulysses exchange reads them from the packed tensor directly). The
+ * backward writes dq, dk, dv into dqkv [B, S, 3, H, D] the same way.
+ * out, lse, dout and every other argument, requirement, the workspace (size
+ * it with usp_attn_{fwd,bwd}_workspace_size(B, S, H, H, D, ...)) and the
+ * errors are those of usp_attn_fwd / usp_attn_bwd.
+ */
+usp_status_t usp_attn_fwd_qkvpacked(const void *qkv, void *out, float *lse,
+                                    int B, int S, int H, int D,
+                                    float softmax_scale, int causal, int window,
+                                    int sink_tokens, const int32_t *cu_seqlens,
+                                    int cp_size, int ulysses_degree,
+                                    usp_layout_t layout, usp_dtype_t dtype,
+                                    unsigned flags, void *workspace,
+                                    size_t workspace_bytes, usp_stream_t stream);
+
+usp_status_t usp_attn_bwd_qkvpacked(const void *qkv, const void *out,
+                                    const float *lse, const void *dout,
+                                    void *dqkv, int B, int S, int H, int D,
+                                    float softmax_scale, int causal, int window,
+                                    int sink_tokens, const int32_t *cu_seqlens,
+                                    int cp_size, int ulysses_degree,
+                                    usp_layout_t layout, usp_dtype_t dtype,
+                                    unsigned flags, void *workspace,
+                                    size_t workspace_bytes, usp_stream_t stream);
+
+/*
  * usp_attn_decode - one decoding step against a KV cache sharded over a ring.
  *
  * "Long Context Attention" notes, "Ring Attention": flash decoding is ring

@@ -178,6 +178,49 @@ def _dims(q: torch.Tensor, k: torch.Tensor, cu_seqlens):
     return B, S, Hq, k.shape[2], D, B
 
 
+def _packed_dims(qkv: torch.Tensor, cu_seqlens):
+    if cu_seqlens is not None:
+        T, _, H, D = qkv.shape
+        return int(cu_seqlens.numel() - 1), T, H, D, 1
+    B, S, _, H, D = qkv.shape
+    return B, S, H, D, B
+
+
+def attn_forward_qkvpacked(qkv, *, causal=True, window=0, sink_tokens=0,
+                           cu_seqlens=None, cp=1, ud=1, layout="contiguous",
+                           softmax_scale=0.0, flags=0, stream=None):
+    """(out, lse) for a packed rank-major qkv [B,S,3,H,D] (packed sequences:
+    [T,3,H,D] with cu_seqlens)."""
+    B, S, H, D, Bl = _packed_dims(qkv, cu_seqlens)
+    out = torch.empty(qkv.shape[:-3] + (H, D), dtype=qkv.dtype, device=qkv.device)
+    lse = torch.empty((Bl, H, S) if cu_seqlens is None else (H, S),
+                      dtype=torch.float32, device=qkv.device)
+    ws_n = usp_attn_fwd_workspace_size(Bl, S, H, H, D, cp, ud, qkv.dtype, flags)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=qkv.device) if ws_n else None
+    _check(_lib.load().usp_attn_fwd_qkvpacked(
+        _p(qkv), _p(out), _p(lse), B, S, H, D, float(softmax_scale), int(causal),
+        int(window), int(sink_tokens), _p(cu_seqlens), cp, ud, _enum(LAYOUT, layout),
+        _enum(DTYPE, qkv.dtype), flags, _p(ws), int(ws_n), _stream(stream)))
+    return out, lse
+
+
+def attn_backward_qkvpacked(qkv, out, lse, dout, *, causal=True, window=0,
+                            sink_tokens=0, cu_seqlens=None, cp=1, ud=1,
+                            layout="contiguous", softmax_scale=0.0, flags=0,
+                            stream=None) -> torch.Tensor:
+    """dqkv (qkv's shape) for a packed qkv and the forward's (out, lse)."""
+    B, S, H, D, Bl = _packed_dims(qkv, cu_seqlens)
+    dqkv = torch.empty_like(qkv)
+    ws_n = usp_attn_bwd_workspace_size(Bl, S, H, H, D, cp, ud, qkv.dtype, flags)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=qkv.device)
+    _check(_lib.load().usp_attn_bwd_qkvpacked(
+        _p(qkv), _p(out), _p(lse), _p(dout), _p(dqkv), B, S, H, D,
+        float(softmax_scale), int(causal), int(window), int(sink_tokens),
+        _p(cu_seqlens), cp, ud, _enum(LAYOUT, layout), _enum(DTYPE, qkv.dtype),
+        flags, _p(ws), int(ws_n), _stream(stream)))
+    return dqkv
+
+
 def attn_decode(q, k, v, *, causal=True, cp=1, splits=1, tree_order=True,
                 softmax_scale=0.0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """(out [B,Tq,Hq,D], lse [B,Tq,Hq]) of the newest Tq tokens q

@@ -226,10 +226,12 @@ bool use_tc_bwd(const AttnParams& P, const Shape& s, unsigned flags) {
 }
 
 // Ulysses exchange of one [B,S,H,D] tensor (row = H*D*elem bytes).
+// tok: elements between tokens of the flat side (0: dense H*D; 3*H*D when
+// the flat side is one of q/k/v (or dq/dk/dv) inside a packed tensor).
 usp_status_t a2a(const void* src, void* dst, const Shape& s, int H, int s2h,
-                 cudaStream_t st) {
+                 cudaStream_t st, long long tok = 0) {
   return launch_ulysses(src, dst, s.B_eff(), s.S, (int)(H * s.D * s.elem()),
-                        s.ud, s2h, st);
+                        s.ud, s2h, st, (int)(tok * s.elem()), 0);
 }
 
 }  // namespace
@@ -326,13 +328,16 @@ size_t usp_attn_bwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
   return c.used;
 }
 
-usp_status_t usp_attn_fwd(const void* q, const void* k, const void* v,
-                          void* out, float* lse, int B, int S, int Hq, int Hkv,
-                          int D, float softmax_scale, int causal, int window,
-                          int sink_tokens, const int32_t* cu_seqlens,
-                          int cp_size, int ulysses_degree, usp_layout_t layout,
-                          usp_dtype_t dtype, unsigned flags, void* workspace,
-                          size_t workspace_bytes, usp_stream_t stream) {
+namespace {
+// tok: elements between tokens of q, k, v (0: dense; 3*Hq*D when they are
+// the three parts of one packed tensor)
+usp_status_t attn_fwd_impl(const void* q, const void* k, const void* v,
+                           void* out, float* lse, int B, int S, int Hq, int Hkv,
+                           int D, float softmax_scale, int causal, int window,
+                           int sink_tokens, const int32_t* cu_seqlens,
+                           int cp_size, int ulysses_degree, usp_layout_t layout,
+                           usp_dtype_t dtype, unsigned flags, void* workspace,
+                           size_t workspace_bytes, usp_stream_t stream, long long tok) {
   Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, dtype,
                      cu_seqlens != nullptr);
   usp_status_t r = validate(s, window, sink_tokens);
@@ -350,12 +355,13 @@ usp_status_t usp_attn_fwd(const void* q, const void* k, const void* v,
   AttnParams P = make_params(s, softmax_scale, causal, window, sink_tokens,
                              cu_seqlens);
   if (s.ud > 1) {
-    if ((r = a2a(q, w.q, s, Hq, 1, st)) != USP_OK) return r;
-    if ((r = a2a(k, w.k, s, Hkv, 1, st)) != USP_OK) return r;
-    if ((r = a2a(v, w.v, s, Hkv, 1, st)) != USP_OK) return r;
-    P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o;
+    if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
+    if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
+    if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
+    P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o;  // dense head groups
   } else {
     P.q = q; P.k = k; P.v = v; P.o = out;
+    P.qkv_tok = tok;
   }
   P.lse = lse;
   if (use_tc_fwd(P, s, flags))
@@ -367,7 +373,39 @@ usp_status_t usp_attn_fwd(const void* q, const void* k, const void* v,
   return r;
 }
 
-usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
+}  // namespace
+
+usp_status_t usp_attn_fwd(const void* q, const void* k, const void* v,
+                          void* out, float* lse, int B, int S, int Hq, int Hkv,
+                          int D, float softmax_scale, int causal, int window,
+                          int sink_tokens, const int32_t* cu_seqlens,
+                          int cp_size, int ulysses_degree, usp_layout_t layout,
+                          usp_dtype_t dtype, unsigned flags, void* workspace,
+                          size_t workspace_bytes, usp_stream_t stream) {
+  return attn_fwd_impl(q, k, v, out, lse, B, S, Hq, Hkv, D, softmax_scale, causal, window,
+                       sink_tokens, cu_seqlens, cp_size, ulysses_degree, layout, dtype, flags,
+                       workspace, workspace_bytes, stream, 0);
+}
+
+usp_status_t usp_attn_fwd_qkvpacked(const void* qkv, void* out, float* lse, int B, int S,
+                                    int H, int D, float softmax_scale, int causal, int window,
+                                    int sink_tokens, const int32_t* cu_seqlens, int cp_size,
+                                    int ulysses_degree, usp_layout_t layout, usp_dtype_t dtype,
+                                    unsigned flags, void* workspace, size_t workspace_bytes,
+                                    usp_stream_t stream) {
+  if (H < 1 || D < 1) return USP_ERR_INVALID_ARG;
+  const size_t part = (size_t)H * D * (dtype == USP_FP32 ? 4 : 2);
+  const char* base = static_cast<const char*>(qkv);
+  return attn_fwd_impl(qkv, base ? base + part : nullptr, base ? base + 2 * part : nullptr, out,
+                       lse, B, S, H, H, D, softmax_scale, causal, window, sink_tokens,
+                       cu_seqlens, cp_size, ulysses_degree, layout, dtype, flags, workspace,
+                       workspace_bytes, stream, 3LL * H * D);
+}
+
+namespace {
+// tok: elements between tokens of q, k, v and dq, dk, dv (0: dense; 3*Hq*D
+// for packed tensors)
+usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
                           const void* out, const float* lse, const void* dout,
                           void* dq, void* dk, void* dv, int B, int S, int Hq,
                           int Hkv, int D, float softmax_scale, int causal,
@@ -375,7 +413,7 @@ usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
                           const int32_t* cu_seqlens, int cp_size,
                           int ulysses_degree, usp_layout_t layout,
                           usp_dtype_t dtype, unsigned flags, void* workspace,
-                          size_t workspace_bytes, usp_stream_t stream) {
+                          size_t workspace_bytes, usp_stream_t stream, long long tok) {
   Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, dtype,
                      cu_seqlens != nullptr);
   usp_status_t r = validate(s, window, sink_tokens);
@@ -394,9 +432,9 @@ usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
   BwdWs w = carve_bwd(c, s, tc);
   if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
   if (s.ud > 1) {
-    if ((r = a2a(q, w.q, s, Hq, 1, st)) != USP_OK) return r;
-    if ((r = a2a(k, w.k, s, Hkv, 1, st)) != USP_OK) return r;
-    if ((r = a2a(v, w.v, s, Hkv, 1, st)) != USP_OK) return r;
+    if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
+    if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
+    if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
     if ((r = a2a(out, w.o, s, Hq, 1, st)) != USP_OK) return r;
     if ((r = a2a(dout, w.dout, s, Hq, 1, st)) != USP_OK) return r;
     P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o; P.dout = w.dout;
@@ -404,6 +442,7 @@ usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
   } else {
     P.q = q; P.k = k; P.v = v; P.o = const_cast<void*>(out); P.dout = dout;
     P.dq = dq; P.dk = dk; P.dv = dv;
+    P.qkv_tok = tok;
   }
   P.lse = const_cast<float*>(lse);
   P.delta = w.delta;
@@ -417,11 +456,43 @@ usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
     r = launch_bwd_simt(P, dtype == USP_BF16, st);
   if (r != USP_OK) return r;
   if (s.ud > 1) {
-    if ((r = a2a(w.dq, dq, s, Hq, 0, st)) != USP_OK) return r;
-    if ((r = a2a(w.dk, dk, s, Hkv, 0, st)) != USP_OK) return r;
-    if ((r = a2a(w.dv, dv, s, Hkv, 0, st)) != USP_OK) return r;
+    if ((r = a2a(w.dq, dq, s, Hq, 0, st, tok)) != USP_OK) return r;
+    if ((r = a2a(w.dk, dk, s, Hkv, 0, st, tok)) != USP_OK) return r;
+    if ((r = a2a(w.dv, dv, s, Hkv, 0, st, tok)) != USP_OK) return r;
   }
   return USP_OK;
+}
+
+}  // namespace
+
+usp_status_t usp_attn_bwd(const void* q, const void* k, const void* v,
+                          const void* out, const float* lse, const void* dout,
+                          void* dq, void* dk, void* dv, int B, int S, int Hq,
+                          int Hkv, int D, float softmax_scale, int causal,
+                          int window, int sink_tokens,
+                          const int32_t* cu_seqlens, int cp_size,
+                          int ulysses_degree, usp_layout_t layout,
+                          usp_dtype_t dtype, unsigned flags, void* workspace,
+                          size_t workspace_bytes, usp_stream_t stream) {
+  return attn_bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, softmax_scale, causal, window, sink_tokens, cu_seqlens, cp_size, ulysses_degree, layout, dtype, flags, workspace, workspace_bytes, stream, 0);
+}
+
+usp_status_t usp_attn_bwd_qkvpacked(const void* qkv, const void* out, const float* lse,
+                                    const void* dout, void* dqkv, int B, int S, int H, int D,
+                                    float softmax_scale, int causal, int window,
+                                    int sink_tokens, const int32_t* cu_seqlens, int cp_size,
+                                    int ulysses_degree, usp_layout_t layout, usp_dtype_t dtype,
+                                    unsigned flags, void* workspace, size_t workspace_bytes,
+                                    usp_stream_t stream) {
+  if (H < 1 || D < 1) return USP_ERR_INVALID_ARG;
+  const size_t part = (size_t)H * D * (dtype == USP_FP32 ? 4 : 2);
+  const char* in = static_cast<const char*>(qkv);
+  char* g = static_cast<char*>(dqkv);
+  return attn_bwd_impl(qkv, in ? in + part : nullptr, in ? in + 2 * part : nullptr, out, lse,
+                       dout, dqkv, g ? g + part : nullptr, g ? g + 2 * part : nullptr, B, S, H,
+                       H, D, softmax_scale, causal, window, sink_tokens, cu_seqlens, cp_size,
+                       ulysses_degree, layout, dtype, flags, workspace, workspace_bytes, stream,
+                       3LL * H * D);
 }
 
 // Decode workspace: the partials [n_part][rows][D] fp32 and [n_part][rows].

@@ -611,14 +611,19 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// dq (bf16) <- dq_acc (fp32), 8 elements per thread-iteration.
+// dq (bf16) <- dq_acc (fp32), 8 elements per thread-iteration. Token rows of
+// row8 8-element groups; dst rows are tok8 groups apart (== row8 when dense,
+// three times it in a packed q/k/v gradient).
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src,
                                                          uint4* __restrict__ dst,
-                                                         long long n8) {
+                                                         long long n8, int row8,
+                                                         long long tok8) {
   for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n8; i += (long long)gridDim.x * 256) {
     const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
-    dst[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
-                        pack_bf16(b.z, b.w));
+    const long long row = i / row8;
+    dst[row * tok8 + (i - row * row8)] =
+        make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
+                   pack_bf16(b.z, b.w));
   }
 }
 
@@ -637,8 +642,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [Bt][S][H][D] -> 4-D map (D, H, S, Bt), box (box0, 1, 128, 1), 128B swizzle;
 // bf16 operand tiles (box0 = 64) or the fp32 dQ accumulator (box0 = 32).
+// tok: elements between tokens (0: dense H*D; 3*H*D in a packed q/k/v tensor)
 bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
-              bool fp32 = false) {
+              bool fp32 = false, long long tok = 0) {
+  if (tok == 0) tok = (long long)H * D;
   auto fn = encode_fn();
   if (!fn) {
     fail_cuda_msg("cuTensorMapEncodeTiled", "driver entry point not found");
@@ -646,8 +653,8 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
   }
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)Bt};
   const cuuint64_t es_b = fp32 ? 4 : 2;
-  cuuint64_t strides[3] = {(cuuint64_t)D * es_b, (cuuint64_t)H * D * es_b,
-                           (cuuint64_t)S * H * D * es_b};
+  cuuint64_t strides[3] = {(cuuint64_t)D * es_b, (cuuint64_t)tok * es_b,
+                           (cuuint64_t)S * tok * es_b};
   cuuint32_t box[4] = {fp32 ? 32u : 64u, 1, (cuuint32_t)kTile, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
@@ -666,10 +673,14 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
 template <int D>
 usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
-  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
-      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D) || !make_map(&mdo, P.dout, P.Bt, P.S, P.Hq, D) ||
+  const long long tok = P.qkv_tok;
+  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D, false, tok) ||
+      !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D, false, tok) ||
+      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D, false, tok) ||
+      !make_map(&mdo, P.dout, P.Bt, P.S, P.Hq, D) ||
       !make_map(&mdq, P.dq_acc, P.Bt, P.S, P.Hq, D, true) ||
-      !make_map(&mdk, P.dk, P.Bt, P.S, P.Hkv, D) || !make_map(&mdv, P.dv, P.Bt, P.S, P.Hkv, D))
+      !make_map(&mdk, P.dk, P.Bt, P.S, P.Hkv, D, false, tok) ||
+      !make_map(&mdv, P.dv, P.Bt, P.S, P.Hkv, D, false, tok))
     return USP_ERR_CUDA;
   static int* status = nullptr;
   if (status == nullptr) {
@@ -705,7 +716,8 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
     ProfScope ps(st, "attn_bwd_dq_convert");
     dq_convert_kernel<<<(unsigned)(n8 < 152LL * 32 * 4 ? (n8 + 255) / 256 : 152 * 16), 256, 0,
                         st>>>(reinterpret_cast<const float4*>(P.dq_acc),
-                              reinterpret_cast<uint4*>(P.dq), n8);
+                              reinterpret_cast<uint4*>(P.dq), n8, P.Hq * D / 8,
+                              qkv_stride(P, P.Hq) / 8);
   }
   note_launch();
   return check_launch();

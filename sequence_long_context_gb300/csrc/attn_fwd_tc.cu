@@ -513,15 +513,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [Bt][S][H][D] bf16 -> 4-D map (D, H, S, Bt), box (64, 1, 128, 1), 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
+// tok: elements between tokens (0: dense H*D; 3*H*D in a packed q/k/v tensor)
+bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
+              long long tok = 0) {
+  if (tok == 0) tok = (long long)H * D;
   auto fn = encode_fn();
   if (!fn) {
     fail_cuda_msg("cuTensorMapEncodeTiled", "driver entry point not found");
     return false;
   }
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)Bt};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
-                           (cuuint64_t)S * H * D * 2};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)tok * 2,
+                           (cuuint64_t)S * tok * 2};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)kBM, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
@@ -540,8 +543,10 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D) {
 template <int D>
 usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D) || !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D) ||
-      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D) || !make_map(&mo, P.o, P.Bt, P.S, P.Hq, D))
+  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D, P.qkv_tok) ||
+      !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D, P.qkv_tok) ||
+      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D, P.qkv_tok) ||
+      !make_map(&mo, P.o, P.Bt, P.S, P.Hq, D))
     return USP_ERR_CUDA;  // detail recorded by make_map
   const int smem = Smem<D>::kAlloc;
   static int* status = nullptr;

@@ -33,9 +33,10 @@ constexpr int kRowsPerBlock = 4;  // warps per block; one row per warp
 
 template <typename T>
 __device__ __forceinline__ const T* row_ptr(const void* base, const AttnParams& P,
-                                            int bt, int p, int h, int H) {
-  return reinterpret_cast<const T*>(base) +
-         (((long long)bt * P.S + p) * H + h) * (long long)P.D;
+                                            int bt, int p, int h, long long tok) {
+  // token stride tok elements: H*D dense, 3*H*D in a packed q/k/v tensor
+  return reinterpret_cast<const T*>(base) + ((long long)bt * P.S + p) * tok +
+         (long long)h * P.D;
 }
 
 // <x, y> over D with x a float row in shared memory and y a tensor row.
@@ -68,7 +69,7 @@ fwd_simt_kernel(AttnParams P) {
   const int g = h / P.G;
   {
     float x[E];
-    load_row<T, E>(row_ptr<T>(P.q, P, bt, row, h, P.Hq) + lane * E, x);
+    load_row<T, E>(row_ptr<T>(P.q, P, bt, row, h, qkv_stride(P, P.Hq)) + lane * E, x);
 #pragma unroll
     for (int e = 0; e < E; ++e) qs[warp][lane * E + e] = x[e] * P.scale_log2;
   }
@@ -89,7 +90,7 @@ fwd_simt_kernel(AttnParams P) {
       const unsigned mask = __ballot_sync(0xffffffffu, vis);
       if (mask == 0u) continue;
       float sc = -INFINITY;
-      if (vis) sc = dot_row<T, D>(qs[warp], row_ptr<T>(P.k, P, bt, kidx, g, P.Hkv));
+      if (vis) sc = dot_row<T, D>(qs[warp], row_ptr<T>(P.k, P, bt, kidx, g, qkv_stride(P, P.Hkv)));
       const float m_new = fmaxf(m, warp_max(sc));
       const float alpha = exp2f(m - m_new);
       const float pj = vis ? exp2f(sc - m_new) : 0.f;
@@ -102,7 +103,7 @@ fwd_simt_kernel(AttnParams P) {
         mm &= mm - 1;
         const float pt = __shfl_sync(0xffffffffu, pj, t);
         float vv[E];
-        load_row<T, E>(row_ptr<T>(P.v, P, bt, kb + t, g, P.Hkv) + lane * E, vv);
+        load_row<T, E>(row_ptr<T>(P.v, P, bt, kb + t, g, qkv_stride(P, P.Hkv)) + lane * E, vv);
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] = fmaf(pt, vv[e], acc[e]);
       }
@@ -112,7 +113,7 @@ fwd_simt_kernel(AttnParams P) {
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] *= inv;
-  T* orow = const_cast<T*>(row_ptr<T>(P.o, P, bt, row, h, P.Hq)) + lane * E;
+  T* orow = const_cast<T*>(row_ptr<T>(P.o, P, bt, row, h, (long long)P.Hq * D)) + lane * E;
   store_row<T, E>(orow, acc);
   if (lane == 0)
     P.lse[lse_index(P, bt, h, row)] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
@@ -168,8 +169,8 @@ bwd_dq_simt_kernel(AttnParams P) {
   const int g = h / P.G;
   {
     float x[E], y[E];
-    load_row<T, E>(row_ptr<T>(P.q, P, bt, row, h, P.Hq) + lane * E, x);
-    load_row<T, E>(row_ptr<T>(P.dout, P, bt, row, h, P.Hq) + lane * E, y);
+    load_row<T, E>(row_ptr<T>(P.q, P, bt, row, h, qkv_stride(P, P.Hq)) + lane * E, x);
+    load_row<T, E>(row_ptr<T>(P.dout, P, bt, row, h, (long long)P.Hq * D) + lane * E, y);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       qs[warp][lane * E + e] = x[e] * P.scale_log2;
@@ -195,9 +196,9 @@ bwd_dq_simt_kernel(AttnParams P) {
       if (mask == 0u) continue;
       float dsj = 0.f;
       if (vis) {
-        const float sc = dot_row<T, D>(qs[warp], row_ptr<T>(P.k, P, bt, kidx, g, P.Hkv));
+        const float sc = dot_row<T, D>(qs[warp], row_ptr<T>(P.k, P, bt, kidx, g, qkv_stride(P, P.Hkv)));
         const float pj = exp2f(sc - lse2);
-        const float dp = dot_row<T, D>(ds[warp], row_ptr<T>(P.v, P, bt, kidx, g, P.Hkv));
+        const float dp = dot_row<T, D>(ds[warp], row_ptr<T>(P.v, P, bt, kidx, g, qkv_stride(P, P.Hkv)));
         dsj = pj * (dp - delta);
       }
       unsigned mm = mask;
@@ -206,7 +207,7 @@ bwd_dq_simt_kernel(AttnParams P) {
         mm &= mm - 1;
         const float w = __shfl_sync(0xffffffffu, dsj, t);
         float kv[E];
-        load_row<T, E>(row_ptr<T>(P.k, P, bt, kb + t, g, P.Hkv) + lane * E, kv);
+        load_row<T, E>(row_ptr<T>(P.k, P, bt, kb + t, g, qkv_stride(P, P.Hkv)) + lane * E, kv);
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] = fmaf(w, kv[e], acc[e]);
       }
@@ -214,7 +215,8 @@ bwd_dq_simt_kernel(AttnParams P) {
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] *= P.scale;
-  T* out = reinterpret_cast<T*>(P.dq) + (((long long)bt * P.S + row) * P.Hq + h) * D + lane * E;
+  T* out = reinterpret_cast<T*>(P.dq) + ((long long)bt * P.S + row) * qkv_stride(P, P.Hq) +
+           (long long)h * D + lane * E;
   store_row<T, E>(out, acc);
 }
 
@@ -230,8 +232,8 @@ bwd_dkdv_simt_kernel(AttnParams P) {
   if (krow >= P.S) return;
   {
     float x[E], y[E];
-    load_row<T, E>(row_ptr<T>(P.k, P, bt, krow, g, P.Hkv) + lane * E, x);
-    load_row<T, E>(row_ptr<T>(P.v, P, bt, krow, g, P.Hkv) + lane * E, y);
+    load_row<T, E>(row_ptr<T>(P.k, P, bt, krow, g, qkv_stride(P, P.Hkv)) + lane * E, x);
+    load_row<T, E>(row_ptr<T>(P.v, P, bt, krow, g, qkv_stride(P, P.Hkv)) + lane * E, y);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       ks[warp][lane * E + e] = x[e] * P.scale_log2;
@@ -261,10 +263,10 @@ bwd_dkdv_simt_kernel(AttnParams P) {
         if (mask == 0u) continue;
         float pj = 0.f, dsj = 0.f;
         if (vis) {
-          const float sc = dot_row<T, D>(ks[warp], row_ptr<T>(P.q, P, bt, qidx, h, P.Hq));
+          const float sc = dot_row<T, D>(ks[warp], row_ptr<T>(P.q, P, bt, qidx, h, qkv_stride(P, P.Hq)));
           const float lse2 = P.lse[lse_index(P, bt, h, qidx)] * kLog2e;
           pj = exp2f(sc - lse2);
-          const float dp = dot_row<T, D>(vs[warp], row_ptr<T>(P.dout, P, bt, qidx, h, P.Hq));
+          const float dp = dot_row<T, D>(vs[warp], row_ptr<T>(P.dout, P, bt, qidx, h, (long long)P.Hq * D));
           const float delta = P.delta[((long long)bt * P.Hq + h) * P.S + qidx];
           dsj = pj * (dp - delta);
         }
@@ -275,8 +277,8 @@ bwd_dkdv_simt_kernel(AttnParams P) {
           const float wp = __shfl_sync(0xffffffffu, pj, t);
           const float wd = __shfl_sync(0xffffffffu, dsj, t);
           float qv[E], dov[E];
-          load_row<T, E>(row_ptr<T>(P.q, P, bt, qb + t, h, P.Hq) + lane * E, qv);
-          load_row<T, E>(row_ptr<T>(P.dout, P, bt, qb + t, h, P.Hq) + lane * E, dov);
+          load_row<T, E>(row_ptr<T>(P.q, P, bt, qb + t, h, qkv_stride(P, P.Hq)) + lane * E, qv);
+          load_row<T, E>(row_ptr<T>(P.dout, P, bt, qb + t, h, (long long)P.Hq * D) + lane * E, dov);
 #pragma unroll
           for (int e = 0; e < E; ++e) {
             dk[e] = fmaf(wd, qv[e], dk[e]);
@@ -288,7 +290,8 @@ bwd_dkdv_simt_kernel(AttnParams P) {
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) dk[e] *= P.scale;
-  const long long off = (((long long)bt * P.S + krow) * P.Hkv + g) * D + lane * E;
+  const long long off =
+      ((long long)bt * P.S + krow) * qkv_stride(P, P.Hkv) + (long long)g * D + lane * E;
   store_row<T, E>(reinterpret_cast<T*>(P.dk) + off, dk);
   store_row<T, E>(reinterpret_cast<T*>(P.dv) + off, dv);
 }

@@ -51,7 +51,15 @@ struct AttnParams {
   int nseq;
   int cp, layout, shard, chunk;
   int unit_batch;    // tensor-core kernels: (batch, head) units per L2 batch
+  // elements between consecutive tokens of q, k, v, dq, dk, dv: 0 = dense
+  // ([.., H, D] rows of H*D); 3*H*D for a packed [B, S, 3, H, D] tensor
+  long long qkv_tok;
 };
+
+// Token stride of q/k/v/dq/dk/dv rows with H heads.
+__host__ __device__ __forceinline__ long long qkv_stride(const AttnParams& P, int H) {
+  return P.qkv_tok ? P.qkv_tok : (long long)H * P.D;
+}
 
 __host__ __device__ __forceinline__ int nat_pos(int p, int layout, int cp,
                                                 int shard, int chunk) {

@@ -72,7 +72,8 @@ permute_layout_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
 // vectors); one warp per (group, token row).
 __global__ void __launch_bounds__(kThreads)
 ulysses_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-               unsigned BS, unsigned rvu, unsigned ud, int seq2head) {
+               unsigned BS, unsigned rvu, unsigned ud, int seq2head,
+               unsigned flat_stride, unsigned flat_off) {
   const unsigned lane = threadIdx.x & 31;
   const unsigned nwarps = gridDim.x * (kThreads / 32);
   const unsigned units = BS * ud;
@@ -80,7 +81,9 @@ ulysses_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
        t += nwarps) {
     const unsigned grp = t / BS, r = t - grp * BS;
     const size_t grouped = (size_t)(grp * BS + r) * rvu;  // [ud][B*S] order
-    const size_t flat = (size_t)(r * ud + grp) * rvu;     // [B*S][ud] order
+    // [B*S][ud] order; a token's row may sit inside a wider one (flat_stride
+    // vectors per token, starting flat_off vectors in: a packed q/k/v tensor)
+    const size_t flat = (size_t)r * flat_stride + flat_off + (size_t)grp * rvu;
     if (seq2head)
       warp_copy(src + flat, dst + grouped, rvu, lane);
     else
@@ -110,15 +113,17 @@ usp_status_t launch_permute_layout(const void* src, void* dst, int B, int S,
 
 usp_status_t launch_ulysses(const void* src, void* dst, int B, int S,
                             int row_bytes, int ud, int seq2head,
-                            cudaStream_t st) {
+                            cudaStream_t st, int flat_row_bytes, int flat_off_bytes) {
   unsigned rvu = (unsigned)(row_bytes / ud / 16);
+  if (flat_row_bytes == 0) flat_row_bytes = row_bytes;
   unsigned BS = (unsigned)B * (unsigned)S;
   if ((long long)BS * rvu * ud == 0) return USP_OK;
   {
     ProfScope ps(st, "permute_ulysses");
     ulysses_kernel<<<grid_for((long long)BS * ud), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
-        BS, rvu, (unsigned)ud, seq2head);
+        BS, rvu, (unsigned)ud, seq2head, (unsigned)(flat_row_bytes / 16),
+        (unsigned)(flat_off_bytes / 16));
   }
   note_launch();
   return check_launch();

@@ -143,3 +143,15 @@ def test_decode_workspace_and_empty_batch(lib):
 def test_selftest_rejects_limits(lib):
     assert lib.usp_selftest_wait_timeout(0, None) == 1
     assert lib.usp_selftest_wait_timeout(2_000_000, None) == 1
+
+
+def test_packed_entry_points_reject_before_launch(lib):
+    # H = 0, a misaligned packed tensor, a missing workspace under Ulysses
+    assert lib.usp_attn_fwd_qkvpacked(FAKE, FAKE, FAKE, 1, 256, 0, 64, 0.0, 1, 0, 0, None, 4, 1,
+                                      1, 1, 0, None, 0, None) == 1
+    assert lib.usp_attn_fwd_qkvpacked(FAKE + 8, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0, 0, None, 4,
+                                      1, 1, 1, 0, None, 0, None) == 3
+    assert lib.usp_attn_fwd_qkvpacked(FAKE, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0, 0, None, 2, 2,
+                                      1, 1, 0, None, 0, None) == 4
+    assert lib.usp_attn_bwd_qkvpacked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0, 0,
+                                      None, 4, 1, 1, 1, 0, None, 0, None) == 4
