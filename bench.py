@@ -203,16 +203,31 @@ def oracle_sample(w, seed: int, budget_s: float):
     return f / dt / 1e12, dt, desc, threads
 
 
+def workload_config(w, total_flop: float, world: int) -> dict:
+    """The `config` object both arms print for workload w."""
+    return {"workload": w.name, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
+            "D": w.D, "layout": w.layout, "cp": w.cp, "ulysses": w.ud,
+            "causal": w.causal, "window": w.window, "sink_tokens": w.sink_tokens,
+            "backward": w.backward,
+            "useful_tflop_per_step": total_flop / 1e12,
+            "parallelism": f"virtual ring cp={w.cp} x ulysses {w.ud} on one GPU; "
+                           f"{world} replica(s)",
+            "l2": "no flush: step inputs larger than L2"}
+
+
 def run_reference(args):
     """The oracle timed on the host cores, as the reference arm."""
     import numpy as np  # noqa: F401
 
-    from sequence_long_context_gb300.workloads import WORKLOADS
+    from sequence_long_context_gb300 import flops
+    from sequence_long_context_gb300.workloads import WORKLOADS, draw_cu_seqlens
 
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
+    cu = draw_cu_seqlens(w.S, w.seg_lo, w.seg_hi, args.seed) if w.varlen else None
+    total = flops.attention_flops(w, cu.tolist() if cu is not None else None)["total"]
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     vals, times = [], []
     desc, thr = "", 0
@@ -227,7 +242,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
+        "config": workload_config(w, total, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -467,14 +482,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "D": w.D, "layout": w.layout, "cp": w.cp, "ulysses": w.ud,
-                   "causal": w.causal, "window": w.window, "sink_tokens": w.sink_tokens,
-                   "backward": w.backward,
-                   "useful_tflop_per_step": F["total"] / 1e12,
-                   "parallelism": f"virtual ring cp={w.cp} x ulysses {w.ud} on one GPU; "
-                                  f"{world} replica(s)",
-                   "l2": "no flush: step inputs larger than L2"},
+        "config": workload_config(w, F["total"], world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches * args.steps), "clocks": clocks,
         "kernels": kernels, "merge": merge_res, "decode": decode_res,
