@@ -285,13 +285,19 @@ def main():
     kw = dict(causal=w.causal, window=w.window, sink_tokens=w.sink_tokens,
               cu_seqlens=cu_dev, cp=w.cp, ud=w.ud, layout=w.layout)
 
+    # one workspace for the forward and the backward of every step: the
+    # backward reads the forward's head-sharded q, k, v, out from it instead
+    # of exchanging them again
+    ws = usp.attn_workspace(x["q"], x["k"], cu_seqlens=cu_dev, cp=w.cp, ud=w.ud)
+
     def step(inp):
         qp, kp, vp = (usp.permute(inp[n], "extract", w.layout, w.cp) for n in "qkv")
-        out, lse = usp.attn_forward(qp, kp, vp, **kw)
+        out, lse = usp.attn_forward(qp, kp, vp, workspace=ws, **kw)
         res = [out]
         if w.backward:
             dop = usp.permute(inp["dout"], "extract", w.layout, w.cp)
-            res += list(usp.attn_backward(qp, kp, vp, out, lse, dop, **kw))
+            res += list(usp.attn_backward(qp, kp, vp, out, lse, dop, workspace=ws,
+                                          saved_exchange=True, **kw))
         return [usp.permute(r, "restore", w.layout, w.cp) for r in res]
 
     def timed(fn, n):

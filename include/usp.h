@@ -90,6 +90,22 @@ typedef enum {
 /* Run the CUDA-core fp32 kernels even where the tensor-core kernels apply
  * (bf16 inputs). Used to cross-check the two kernel families. */
 #define USP_FLAG_FORCE_SIMT 1u
+/* usp_attn_bwd / usp_attn_bwd_qkvpacked with ulysses_degree > 1: reuse the
+ * forward's Ulysses exchange instead of redoing it. The backward of the
+ * method keeps the head-sharded q, k, v, output and LSE of the forward
+ * ("Long Context Attention" notes, "Motivation": QKV, output, LSE and dout
+ * are stored for the backward), so only dout goes through the sequence-to-
+ * head exchange and dq, dk, dv through the way back. The caller passes the
+ * backward the same workspace that the forward call with the same arguments
+ * wrote (so it must be at least usp_attn_bwd_workspace_size bytes, which is
+ * never less than the forward's size), untouched since: its first
+ * usp_attn_fwd_workspace_size bytes then hold the forward's head-sharded
+ * q, k, v and out, where the backward reads them. q, k, v, out are not read
+ * and may be NULL. Ignored by the forward and when ulysses_degree == 1;
+ * rejected (USP_ERR_INVALID_ARG) by usp_attn_bwd_noalloc. The contents of
+ * the workspace are trusted: a workspace that does not hold that forward's
+ * exchange gives wrong gradients, not an error. */
+#define USP_FLAG_SAVED_EXCHANGE 2u
 
 /*
  * usp_attn_fwd - ring attention forward with the fused LSE merge.
@@ -127,7 +143,9 @@ typedef enum {
  * flags  USP_FLAG_*.
  * workspace / workspace_bytes  caller scratch of at least
  *      usp_attn_fwd_workspace_size(...) bytes, 256-byte aligned (may be NULL
- *      when that size is 0). Its contents on entry are irrelevant.
+ *      when that size is 0). Its contents on entry are irrelevant. With
+ *      ulysses_degree > 1 it holds the head-sharded q, k, v and out on
+ *      return (what USP_FLAG_SAVED_EXCHANGE lets the backward reuse).
  * Errors: USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, USP_ERR_WORKSPACE,
  *      USP_ERR_UNSUPPORTED (fp32 with D not in {64,128}), USP_ERR_CUDA.
  */
@@ -155,7 +173,9 @@ size_t usp_attn_fwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
  * contributions of every query rank that saw it (the shard's ring return)
  * and of all Hq/Hkv query heads sharing the KV head.
  *
- * q, k, v, out, lse: as passed to / produced by usp_attn_fwd (same args).
+ * q, k, v, out, lse: as passed to / produced by usp_attn_fwd (same args);
+ *      with USP_FLAG_SAVED_EXCHANGE and ulysses_degree > 1, q, k, v, out are
+ *      read from the forward's workspace instead (see the flag).
  * dout [B,S,Hq,D] rank-major, dtype as q. dq/dk/dv written, shapes of q/k/v.
  * Scalar arguments must equal those of the forward call.
  * Errors: as usp_attn_fwd.

@@ -21,6 +21,7 @@ LAYOUT = {"contiguous": 0, "zigzag": 1, "stripe": 2}
 DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 PERMUTE = {"extract": 0, "restore": 1, "seq2head": 2, "head2seq": 3}
 FLAG_FORCE_SIMT = 1
+FLAG_SAVED_EXCHANGE = 2
 
 
 class UspError(RuntimeError):
@@ -188,15 +189,16 @@ def _packed_dims(qkv: torch.Tensor, cu_seqlens):
 
 def attn_forward_qkvpacked(qkv, *, causal=True, window=0, sink_tokens=0,
                            cu_seqlens=None, cp=1, ud=1, layout="contiguous",
-                           softmax_scale=0.0, flags=0, stream=None):
+                           softmax_scale=0.0, flags=0, workspace=None, stream=None):
     """(out, lse) for a packed rank-major qkv [B,S,3,H,D] (packed sequences:
     [T,3,H,D] with cu_seqlens)."""
     B, S, H, D, Bl = _packed_dims(qkv, cu_seqlens)
     out = torch.empty(qkv.shape[:-3] + (H, D), dtype=qkv.dtype, device=qkv.device)
     lse = torch.empty((Bl, H, S) if cu_seqlens is None else (H, S),
                       dtype=torch.float32, device=qkv.device)
-    ws_n = usp_attn_fwd_workspace_size(Bl, S, H, H, D, cp, ud, qkv.dtype, flags)
-    ws = torch.empty(ws_n, dtype=torch.uint8, device=qkv.device) if ws_n else None
+    ws, ws_n = _use_workspace(
+        workspace, usp_attn_fwd_workspace_size(Bl, S, H, H, D, cp, ud, qkv.dtype, flags),
+        qkv.device)
     _check(_lib.load().usp_attn_fwd_qkvpacked(
         _p(qkv), _p(out), _p(lse), B, S, H, D, float(softmax_scale), int(causal),
         int(window), int(sink_tokens), _p(cu_seqlens), cp, ud, _enum(LAYOUT, layout),
@@ -207,12 +209,19 @@ def attn_forward_qkvpacked(qkv, *, causal=True, window=0, sink_tokens=0,
 def attn_backward_qkvpacked(qkv, out, lse, dout, *, causal=True, window=0,
                             sink_tokens=0, cu_seqlens=None, cp=1, ud=1,
                             layout="contiguous", softmax_scale=0.0, flags=0,
+                            workspace=None, saved_exchange=False,
                             stream=None) -> torch.Tensor:
-    """dqkv (qkv's shape) for a packed qkv and the forward's (out, lse)."""
+    """dqkv (qkv's shape) for a packed qkv and the forward's (out, lse);
+    saved_exchange as in attn_backward."""
     B, S, H, D, Bl = _packed_dims(qkv, cu_seqlens)
     dqkv = torch.empty_like(qkv)
-    ws_n = usp_attn_bwd_workspace_size(Bl, S, H, H, D, cp, ud, qkv.dtype, flags)
-    ws = torch.empty(ws_n, dtype=torch.uint8, device=qkv.device)
+    if saved_exchange:
+        if workspace is None:
+            raise ValueError("saved_exchange needs the forward's workspace")
+        flags |= FLAG_SAVED_EXCHANGE
+    ws, ws_n = _use_workspace(
+        workspace, usp_attn_bwd_workspace_size(Bl, S, H, H, D, cp, ud, qkv.dtype, flags),
+        qkv.device)
     _check(_lib.load().usp_attn_bwd_qkvpacked(
         _p(qkv), _p(out), _p(lse), _p(dout), _p(dqkv), B, S, H, D,
         float(softmax_scale), int(causal), int(window), int(sink_tokens),
@@ -236,17 +245,36 @@ def attn_decode(q, k, v, *, causal=True, cp=1, splits=1, tree_order=True,
     return out, lse
 
 
+def _use_workspace(workspace, need, device):
+    """The caller's uint8 workspace (checked for size), else a fresh one."""
+    if workspace is None:
+        return torch.empty(need, dtype=torch.uint8, device=device) if need else None, need
+    if workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    return workspace, workspace.numel()
+
+
+def attn_workspace(q, k, *, cu_seqlens=None, cp=1, ud=1, flags=0) -> torch.Tensor:
+    """A workspace that fits both attn_forward and attn_backward of these
+    shapes. Passing the same one to both, and saved_exchange=True to the
+    backward, lets the backward reuse the forward's Ulysses exchange."""
+    B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
+    n = usp_attn_bwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags)
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
 def attn_forward(q, k, v, *, causal=True, window=0, sink_tokens=0,
                  cu_seqlens=None, cp=1, ud=1, layout="contiguous",
-                 softmax_scale=0.0, flags=0, stream=None
+                 softmax_scale=0.0, flags=0, workspace=None, stream=None
                  ) -> Tuple[torch.Tensor, torch.Tensor]:
     """(out, lse) for rank-major q/k/v ([B,S,H,D] or packed [T,H,D])."""
     B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
     out = torch.empty_like(q)
     lse = torch.empty((Bl, Hq, S) if cu_seqlens is None else (Hq, S),
                       dtype=torch.float32, device=q.device)
-    ws_n = usp_attn_fwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags)
-    ws = torch.empty(ws_n, dtype=torch.uint8, device=q.device) if ws_n else None
+    ws, ws_n = _use_workspace(
+        workspace, usp_attn_fwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags),
+        q.device)
     usp_attn_fwd(q, k, v, out, lse, B, S, Hq, Hkv, D, softmax_scale, causal,
                  window, sink_tokens, cu_seqlens, cp, ud, layout, q.dtype,
                  flags, ws, ws_n, stream)
@@ -256,12 +284,19 @@ def attn_forward(q, k, v, *, causal=True, window=0, sink_tokens=0,
 def attn_backward(q, k, v, out, lse, dout, *, causal=True, window=0,
                   sink_tokens=0, cu_seqlens=None, cp=1, ud=1,
                   layout="contiguous", softmax_scale=0.0, flags=0,
-                  stream=None):
-    """(dq, dk, dv) for rank-major tensors and the forward's (out, lse)."""
+                  workspace=None, saved_exchange=False, stream=None):
+    """(dq, dk, dv) for rank-major tensors and the forward's (out, lse).
+    saved_exchange: workspace is the one the forward wrote (attn_workspace),
+    holding its head-sharded q, k, v, out (FLAG_SAVED_EXCHANGE)."""
     B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_n = usp_attn_bwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags)
-    ws = torch.empty(ws_n, dtype=torch.uint8, device=q.device)
+    if saved_exchange:
+        if workspace is None:
+            raise ValueError("saved_exchange needs the forward's workspace")
+        flags |= FLAG_SAVED_EXCHANGE
+    ws, ws_n = _use_workspace(
+        workspace, usp_attn_bwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags),
+        q.device)
     usp_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D,
                  softmax_scale, causal, window, sink_tokens, cu_seqlens, cp,
                  ud, layout, q.dtype, flags, ws, ws_n, stream)

@@ -190,18 +190,23 @@ struct BwdWs {
   float* dq_acc;
   void *q, *k, *v, *o, *dout, *dq, *dk, *dv;
 };
+// The head-sharded q, k, v, o come first, at carve_fwd's offsets, so that a
+// forward's workspace handed to the backward (USP_FLAG_SAVED_EXCHANGE) still
+// holds them where the backward reads them.
 BwdWs carve_bwd(Carve& c, const Shape& s, bool tc) {
   BwdWs w{};
+  if (s.ud > 1) {
+    w.q = c.take(s.q_bytes());
+    w.k = c.take(s.kv_bytes());
+    w.v = c.take(s.kv_bytes());
+    w.o = c.take(s.q_bytes());
+  }
   w.delta = static_cast<float*>(c.take((size_t)s.B_eff() * s.Hq * s.S * 4));
   if (tc) {
     w.lse2 = static_cast<float*>(c.take((size_t)s.B_eff() * s.Hq * s.S * 4));
     w.dq_acc = static_cast<float*>(c.take((size_t)s.B_eff() * s.S * s.Hq * s.D * 4));
   }
   if (s.ud > 1) {
-    w.q = c.take(s.q_bytes());
-    w.k = c.take(s.kv_bytes());
-    w.v = c.take(s.kv_bytes());
-    w.o = c.take(s.q_bytes());
     w.dout = c.take(s.q_bytes());
     w.dq = c.take(s.q_bytes());
     w.dk = c.take(s.kv_bytes());
@@ -418,7 +423,9 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
                      cu_seqlens != nullptr);
   usp_status_t r = validate(s, window, sink_tokens);
   if (r != USP_OK) return r;
-  if (S > 0 && (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv))
+  // saved: the workspace holds the forward's head-sharded q, k, v, out
+  const bool saved = (flags & USP_FLAG_SAVED_EXCHANGE) && s.ud > 1;
+  if (S > 0 && (!lse || !dout || !dq || !dk || !dv || (!saved && (!q || !k || !v || !out))))
     return USP_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv, workspace};
   for (const void* p : ptrs)
@@ -432,10 +439,12 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
   BwdWs w = carve_bwd(c, s, tc);
   if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
   if (s.ud > 1) {
-    if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
-    if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
-    if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
-    if ((r = a2a(out, w.o, s, Hq, 1, st)) != USP_OK) return r;
+    if (!saved) {
+      if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
+      if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
+      if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
+      if ((r = a2a(out, w.o, s, Hq, 1, st)) != USP_OK) return r;
+    }
     if ((r = a2a(dout, w.dout, s, Hq, 1, st)) != USP_OK) return r;
     P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o; P.dout = w.dout;
     P.dq = w.dq; P.dk = w.dk; P.dv = w.dv;

@@ -67,6 +67,11 @@ usp_status_t usp_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                                   int ulysses_degree, usp_layout_t layout,
                                   usp_dtype_t dtype, unsigned flags,
                                   usp_stream_t stream) {
+  if (flags & USP_FLAG_SAVED_EXCHANGE) {
+    set_error_detail("usp_attn_bwd_noalloc: USP_FLAG_SAVED_EXCHANGE needs the "
+                     "forward's workspace, which this call does not take");
+    return USP_ERR_INVALID_ARG;
+  }
   // Packed batches keep one leading batch row in their tensors.
   const int b_tensor = cu_seqlens != nullptr ? 1 : B;
   const size_t need = usp_attn_bwd_workspace_size(

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import __graft_entry__
 import sequence_long_context_gb300 as usp
@@ -155,3 +156,51 @@ def test_packed_entry_points_reject_before_launch(lib):
                                       1, 1, 0, None, 0, None) == 4
     assert lib.usp_attn_bwd_qkvpacked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0, 0,
                                       None, 4, 1, 1, 1, 0, None, 0, None) == 4
+
+
+def bwd(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             B=1, S=256, Hq=4, Hkv=2, D=64, scale=0.0, causal=1, window=0, sink=0, cu=None,
+             cp=2, ud=2, layout=1, dtype=1, flags=0, ws=None, wsb=0, stream=None)
+    a.update(over)
+    return lib.usp_attn_bwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["dout"], a["dq"],
+                            a["dk"], a["dv"], a["B"], a["S"], a["Hq"], a["Hkv"], a["D"],
+                            a["scale"], a["causal"], a["window"], a["sink"], a["cu"], a["cp"],
+                            a["ud"], a["layout"], a["dtype"], a["flags"], a["ws"], a["wsb"],
+                            a["stream"])
+
+
+def test_saved_exchange_flag_host_checks(lib):
+    F = usp.FLAG_SAVED_EXCHANGE
+    none = dict(q=None, k=None, v=None, out=None)
+    # with the flag under Ulysses, q/k/v/out are not needed: the call gets as
+    # far as the (missing) workspace
+    assert bwd(lib, flags=F, **none) == 4
+    # without Ulysses the flag does nothing, so the null tensors are an error
+    assert bwd(lib, flags=F, ud=1, **none) == 1
+    assert bwd(lib, flags=0, **none) == 1
+    # the no-alloc call has no forward workspace to read from
+    st = lib.usp_attn_bwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  1, 256, 4, 2, 64, 0.0, 1, 0, 0, None, 2, 2, 1, 1, F, None)
+    assert st == 1
+    assert b"SAVED_EXCHANGE" in lib.usp_last_error_detail()
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,cp,ud,dtype", [
+    (2, 8192, 32, 32, 128, 4, 2, 1), (1, 4096, 32, 8, 128, 2, 4, 1), (1, 512, 4, 2, 64, 2, 2, 0),
+    (3, 1000, 8, 8, 64, 1, 8, 0)])
+def test_backward_workspace_holds_the_forward_exchange(lib, B, S, Hq, Hkv, D, cp, ud, dtype):
+    # the saved-exchange flag relies on the forward's workspace being a
+    # prefix of the backward's (same q, k, v, o slices at the same offsets)
+    f = usp.usp_attn_fwd_workspace_size(B, S, Hq, Hkv, D, cp, ud, dtype)
+    b = usp.usp_attn_bwd_workspace_size(B, S, Hq, Hkv, D, cp, ud, dtype)
+    el = 2 if dtype == 0 else 4
+    assert f == 2 * B * S * (Hq + Hkv) * D * el
+    assert b >= f
+
+
+def test_python_saved_exchange_needs_the_workspace():
+    q = torch.zeros(1, 256, 4, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        usp.attn_backward(q, k, k, q, None, q, cp=2, ud=2, saved_exchange=True)
