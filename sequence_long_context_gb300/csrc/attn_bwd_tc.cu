@@ -20,12 +20,14 @@
 //              memory (A operand of dQ)
 //   warps 8-11 dQ group, one query row per thread: takes the dQ tile out of
 //              tensor memory (freeing it for the next tile's dP^T), stages
-//              it in the tile's Q/dO ring slot once the tile's dV/dK MMAs
-//              are done with it, and has the TMA unit add it into the global
-//              fp32 accumulator; the slot goes back to the producer once the
-//              TMA has read it
-//   warp 12    producer: K, V once; then Q, dO tiles through a 2-slot ring
-//              (a slot is refilled after the dQ drain hands it back)
+//              it in the dS tile and the dO half of the tile's ring slot
+//              (both dead once the tile's dQ MMA is done), and has the TMA
+//              unit add it into the global fp32 accumulator; the dS tile
+//              and the dO half go back once the TMA has read them
+//   warp 12    producer: K, V once; then Q, dO tiles through a 2-slot ring.
+//              The Q half of a slot (Q tile, LSE and Delta rows) is refilled
+//              as soon as the tile's last MMA (dK, which reads Q) is done;
+//              the dO half once the dQ drain hands it back
 //   warp 13    MMA issuer and tensor-memory owner
 // Tensor memory (512 columns): S^T [0,128); queries 64g..64g+63 (softmax
 // group g) live in columns [64g, 64g+64) and are overwritten in place by
@@ -71,12 +73,13 @@ struct BSmem {
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
                        kDKVFull = 12, kMmaDone = 13, kPReady = 14, kDQGroup = 15,
-                       kStageFree = 16, kDOFull = 18, kStageFreeDO = 20, kKVStaged = 22,
-                       kNumBars = 24;
+                       kDSFree = 16, kDOFull = 17, kStageFreeDO = 19, kKVStaged = 21,
+                       kNumBars = 23;
   // Each Q/dO slot has two halves with their own full/free barriers: the Q
-  // half (Q tile, LSE and Delta rows; kQFull / kStageFree) and the dO half
-  // (kDOFull / kStageFreeDO). The dQ drain stages through both and frees the
-  // Q half first, so the next tile's Q and S^T need not wait for the rest.
+  // half (Q tile, LSE and Delta rows; kQFull / kQEmpty, the commit of the
+  // tile's last MMA) and the dO half (kDOFull / kStageFreeDO, handed back by
+  // the dQ drain, which stages through it). kDSFree: the dS tile may take
+  // the next tile's dS (the drain's staging in it has been read).
   // 16-byte aligned: int4 / float4 accesses below
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
@@ -158,11 +161,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kDQFull), 1);
     mbar_init(bar(L::kDQEmpty), kTile / 32);  // one arrival per drain warp
     mbar_init(bar(L::kDQGroup), kTile);
-    for (int s = 0; s < 2; ++s) {  // Q/dO slot halves handed back by the dQ drain
-      mbar_init(bar(L::kStageFree + s), 1);
+    for (int s = 0; s < 2; ++s) {  // dO halves, handed back by the dQ drain
       mbar_init(bar(L::kStageFreeDO + s), 1);
       mbar_init(bar(L::kDOFull + s), 1);
     }
+    mbar_init(bar(L::kDSFree), 1);
     mbar_init(bar(L::kInfoS), 1);
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
@@ -214,9 +217,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           for (int hh = 0; hh < P.G && ok; ++hh) {
             const int h = g * P.G + hh;
             const int slot = n & 1, use = n >> 1;
-            // each half of the slot is free once the dQ drain has used it
-            // as staging
-            if (use >= 1 && !(ok = mbar_wait(bar(L::kStageFree + slot), (use - 1) & 1,
+            // the Q half is free once the MMAs of its previous tile are done;
+            // the dO half once the dQ drain has used it as staging
+            if (use >= 1 && !(ok = mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1,
                                              abort_flag, P.status)))
               break;
             sched[slot] = make_int4(qt, h, cls, 0);
@@ -244,13 +247,13 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       }
       if (ok) {
         const int slot = n & 1, use = n >> 1;
-        if (use < 1 || mbar_wait(bar(L::kStageFree + slot), (use - 1) & 1, abort_flag,
+        if (use < 1 || mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1, abort_flag,
                                  P.status)) {
           sched[slot] = make_int4(kEnd, 0, 0, 0);
           mbar_arrive(bar(L::kQFull + slot));
         }
         for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
-          if (!mbar_wait(bar(L::kStageFree + (m & 1)), (m >> 1) & 1, abort_flag, P.status) ||
+          if (!mbar_wait(bar(L::kQEmpty + (m & 1)), (m >> 1) & 1, abort_flag, P.status) ||
               !mbar_wait(bar(L::kStageFreeDO + (m & 1)), (m >> 1) & 1, abort_flag, P.status))
             break;
       }
@@ -419,8 +422,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kPReady));
       ok = mbar_wait(bar(L::kDPFull), c & 1, abort_flag, P.status);
-      // the dS buffer is still read by the previous tile's dQ MMAs
-      if (ok && c > 0) ok = mbar_wait(bar(L::kDQFull), (c - 1) & 1, abort_flag, P.status);
+      // the dS tile holds the previous tile's dQ staging until the TMA has
+      // read it (and before that its dS, read by that tile's dQ MMA)
+      if (ok && c > 0) ok = mbar_wait(bar(L::kDSFree), (c - 1) & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       tmem_wait_st();
@@ -528,13 +532,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_wait_ld();
     };
-    // staging box cg (32 fp32 columns x 128 rows, 16 KB) of a Q/dO slot: the
-    // first D/64 boxes fill the Q tile's space, the rest the dO tile's
+    // staging box cg (32 fp32 columns x 128 rows, 16 KB): the first two fill
+    // the dS tile (32 KB), the rest the dO half of the tile's slot
+    constexpr int kBoxBytes = kTile * 128;
+    constexpr int kBoxes = D / 32;
+    constexpr int kBoxesInDS = kBoxes < 2 ? kBoxes : 2;
+    static_assert(kBoxesInDS * kBoxBytes <= kTile * kTile * 2, "staging exceeds the dS tile");
+    static_assert((kBoxes - kBoxesInDS) * kBoxBytes <= L::kTileBytes,
+                  "staging exceeds the dO half");
     auto stage_box = [&](int slot, int cg) -> uint8_t* {
-      constexpr int kBoxBytes = kTile * 128;
-      constexpr int kBoxesInQ = L::kTileBytes / kBoxBytes;
-      return cg < kBoxesInQ ? sm + L::kQ + slot * L::kTileBytes + cg * kBoxBytes
-                            : sm + L::kDO + slot * L::kTileBytes + (cg - kBoxesInQ) * kBoxBytes;
+      return cg < kBoxesInDS ? sm + L::kDS + cg * kBoxBytes
+                             : sm + L::kDO + slot * L::kTileBytes + (cg - kBoxesInDS) * kBoxBytes;
     };
     const bool leader = qw == 0 && lane == 0;  // issues the reductions
     auto release_tmem = [&]() {  // every dQ column has been read
@@ -551,17 +559,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // This tile's Q/dO ring slot is free once its dV/dK MMAs are done and
-      // stays free until the producer refills it for two tiles later: dQ is
-      // staged there, scaled, as D/32 boxes of 32 fp32 columns x 128 rows in
-      // the 128-byte swizzle (16-byte chunk k of row r at k ^ (r & 7)), and
-      // one thread hands the boxes to the TMA unit, which adds them into the
-      // global fp32 accumulator. The slot goes back to the producer as soon
-      // as the TMA has read it; the additions complete asynchronously.
+      // Once this tile's dQ MMA is done, nothing reads its dS tile or the dO
+      // half of its slot any more (the dP^T and dV MMAs that read dO were
+      // issued before it), and neither is written again before this drain
+      // hands it back: dQ is staged there, scaled, as D/32 boxes of 32 fp32
+      // columns x 128 rows in the 128-byte swizzle (16-byte chunk k of row r
+      // at k ^ (r & 7)), and one thread hands the boxes to the TMA unit,
+      // which adds them into the global fp32 accumulator. Each space goes
+      // back as soon as the TMA has read it; the additions complete
+      // asynchronously. The Q half of the slot is not used, so the producer
+      // can refill it as soon as the tile's dK MMA is done.
       const int slot = c & 1;
-      ok = mbar_wait(bar(L::kQEmpty + slot), (c >> 1) & 1, abort_flag, P.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
         uint32_t v[64];
@@ -585,18 +593,22 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       fence_proxy_async_smem();
       if (!(ok = group_sync(L::kDQGroup, c))) break;  // all rows staged
       if (leader) {
-        // the Q half's boxes first, as their own bulk group: that half is
-        // handed back as soon as the TMA has read it
-        constexpr int kBoxesInQ = D / 64;
+        // the dS tile's boxes first, as their own bulk group: the softmax
+        // waits for that space before it writes the next tile's dS
 #pragma unroll
-        for (int cg = 0; cg < D / 32; ++cg) {
+        for (int cg = 0; cg < kBoxes; ++cg) {
           tma_reduce_add_4d(&tm_dq, smem_u32(stage_box(slot, cg)), 32 * cg, h, qt * kTile, bt);
-          if (cg + 1 == kBoxesInQ) bulk_commit_group();
+          if (cg + 1 == kBoxesInDS && kBoxesInDS < kBoxes) bulk_commit_group();
         }
         bulk_commit_group();
-        bulk_wait_group_read1();
-        mbar_arrive(bar(L::kStageFree + slot));
-        bulk_wait_group_read0();
+        if constexpr (kBoxesInDS < kBoxes) {
+          bulk_wait_group_read1();
+          mbar_arrive(bar(L::kDSFree));
+          bulk_wait_group_read0();
+        } else {
+          bulk_wait_group_read0();
+          mbar_arrive(bar(L::kDSFree));
+        }
         mbar_arrive(bar(L::kStageFreeDO + slot));
       }
       ++c;
