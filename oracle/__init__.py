@@ -14,10 +14,12 @@ Modules
   ring       a ring simulator: per-chunk partials in ring order + merge
   decode     a decode step: the newest tokens against a sharded KV cache,
              and the per-shard partials that a tree merge combines
+  fp8        E4M3 codes (encode / decode / per-tensor quantization) and the
+             attention of e4m3 q, k, v with per-tensor descales
 
 Every function is pinned by `-m "not gpu"` tests against something other than
 itself (brute force, a library routine, finite differences, closed forms and
 the worked examples printed on the pages). No function here is "parity
 unpinned".
 """
-from . import attention, layouts, merge, ring  # noqa: F401
+from . import attention, decode, fp8, layouts, merge, ring  # noqa: F401
