@@ -288,6 +288,61 @@ usp_status_t usp_attn_bwd_qkvpacked(const void *qkv, const void *out,
                                     size_t workspace_bytes, usp_stream_t stream);
 
 /*
+ * usp_attn_fwd_fp8 - usp_attn_fwd on 8-bit float (E4M3) q, k, v.
+ *
+ * The USP README ("3. Test") runs a forward-only fp8 attention backend
+ * under the same sequence-parallel wrappers; the pages give no arithmetic
+ * for it. This call computes the attention of usp_attn_fwd (same masks,
+ * GQA, varlen, ring schedule, layouts and Ulysses exchange) of the real
+ * values e4m3(code) * descale, with one descale per tensor:
+ *   s_ij = softmax_scale * <q_i, k_j>   (real values),
+ *   O_i = sum_j exp(s_ij - LSE_i) v_j,  LSE_i = log sum_j exp(s_ij).
+ * Both products run on the tensor cores on the codes (fp32 accumulation);
+ * the probabilities are rounded to E4M3 (as codes of 16 p) for the P V
+ * product, which the result's tolerance has to cover; LSE is taken from the
+ * unrounded fp32 probabilities.
+ *
+ * q [B,S,Hq,128], k, v [B,S,Hkv,128]: E4M3 codes (OCP 8-bit float, E4M3:
+ *      bias 7, largest finite 448, 0x7F / 0xFF NaN), rank-major as in
+ *      usp_attn_fwd (packed [T,H,128] with cu_seqlens), 16-byte aligned.
+ * q_descale, k_descale, v_descale  finite, > 0 (else USP_ERR_INVALID_ARG).
+ * out  [B,S,Hq,128] bf16, written.  lse  as in usp_attn_fwd.
+ * Other arguments as in usp_attn_fwd (dtype is implied; flags unused).
+ * workspace  at least usp_attn_fwd_fp8_workspace_size(...) bytes, 16-byte
+ *      aligned, never NULL for S > 0 (it holds V transposed to
+ *      [B][Hkv][128][S]); contents on entry irrelevant.
+ * Errors: as usp_attn_fwd; USP_ERR_UNSUPPORTED for a head dim other than
+ *      128 or a shard / zigzag chunk that is not a multiple of 256 tokens.
+ */
+usp_status_t usp_attn_fwd_fp8(const void *q, const void *k, const void *v,
+                              float q_descale, float k_descale, float v_descale,
+                              void *out, float *lse, int B, int S, int Hq, int Hkv,
+                              int D, float softmax_scale, int causal, int window,
+                              int sink_tokens, const int32_t *cu_seqlens,
+                              int cp_size, int ulysses_degree, usp_layout_t layout,
+                              unsigned flags, void *workspace, size_t workspace_bytes,
+                              usp_stream_t stream);
+
+/* Bytes of scratch usp_attn_fwd_fp8 needs (B: the tensors' batch rows, 1
+ * for packed sequences); 0 for invalid sizes. */
+size_t usp_attn_fwd_fp8_workspace_size(int B, int S, int Hq, int Hkv, int D,
+                                       int cp_size, int ulysses_degree);
+
+/*
+ * usp_quantize_e4m3 - out[i] = E4M3 code of x[i] * inv_scale.
+ *
+ * x  n bf16 values (device, 16-byte aligned); out  n codes (device,
+ * 16-byte aligned). The product is taken in fp32 (rounded to nearest) and
+ * rounded to the nearest code, ties to the even code; finite values beyond
+ * 448 saturate to +-448, NaN stays NaN. The matching descale for
+ * usp_attn_fwd_fp8 is 1 / inv_scale. Errors: USP_ERR_INVALID_ARG (n < 0,
+ * NULL pointers with n > 0, inv_scale not finite), USP_ERR_ALIGNMENT,
+ * USP_ERR_CUDA.
+ */
+usp_status_t usp_quantize_e4m3(const void *x, void *out, int64_t n, float inv_scale,
+                               usp_stream_t stream);
+
+/*
  * usp_attn_decode - one decoding step against a KV cache sharded over a ring.
  *
  * "Long Context Attention" notes, "Ring Attention": flash decoding is ring
@@ -341,7 +396,7 @@ size_t usp_attn_decode_workspace_size(int B, int Tq, int S, int Hq, int Hkv,
  *     src [B, S, H, D] rank-major -> dst [ud, B, S, H/ud, D] with
  *     dst[u][b][p][h][d] = src[b][p][u*H/ud + h][d].
  * ULYSSES_HEAD2SEQ is its inverse (dst [B,S,H,D], src [ud,B,S,H/ud,D]).
- * elem_bytes 2 or 4. H*D*elem_bytes (Ulysses: H/ud*D*elem_bytes) must be a
+ * elem_bytes 1 (E4M3 codes), 2 or 4. H*D*elem_bytes (Ulysses: H/ud*D*elem_bytes) must be a
  * multiple of 16. S divisible as for usp_attn_fwd. src and dst must not
  * overlap. Errors: USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, USP_ERR_CUDA.
  */

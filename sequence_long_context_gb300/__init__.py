@@ -71,6 +71,27 @@ def usp_attn_fwd(q, k, v, out, lse, B, S, Hq, Hkv, D, softmax_scale, causal,
         _stream(stream)))
 
 
+def usp_attn_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, out, lse, B, S, Hq, Hkv,
+                     D, softmax_scale, causal, window, sink_tokens, cu_seqlens, cp_size,
+                     ulysses_degree, layout, flags=0, workspace=None, workspace_bytes=0,
+                     stream=None) -> None:
+    _check(_lib.load().usp_attn_fwd_fp8(
+        _p(q), _p(k), _p(v), float(q_descale), float(k_descale), float(v_descale), _p(out),
+        _p(lse), B, S, Hq, Hkv, D, float(softmax_scale), int(causal), int(window),
+        int(sink_tokens), _p(cu_seqlens), cp_size, ulysses_degree, _enum(LAYOUT, layout),
+        flags, _p(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def usp_attn_fwd_fp8_workspace_size(B, S, Hq, Hkv, D, cp_size, ulysses_degree) -> int:
+    return int(_lib.load().usp_attn_fwd_fp8_workspace_size(B, S, Hq, Hkv, D, cp_size,
+                                                           ulysses_degree))
+
+
+def usp_quantize_e4m3(x, out, n, inv_scale, stream=None) -> None:
+    _check(_lib.load().usp_quantize_e4m3(_p(x), _p(out), int(n), float(inv_scale),
+                                         _stream(stream)))
+
+
 def usp_attn_fwd_workspace_size(B, S, Hq, Hkv, D, cp_size, ulysses_degree,
                                 dtype, flags=0) -> int:
     return int(_lib.load().usp_attn_fwd_workspace_size(
@@ -301,6 +322,34 @@ def attn_backward(q, k, v, out, lse, dout, *, causal=True, window=0,
                  softmax_scale, causal, window, sink_tokens, cu_seqlens, cp,
                  ud, layout, q.dtype, flags, ws, ws_n, stream)
     return dq, dk, dv
+
+
+def quantize_e4m3(x: torch.Tensor, inv_scale: float, stream=None) -> torch.Tensor:
+    """E4M3 codes (uint8, x's shape) of a bf16 tensor times inv_scale."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("quantize_e4m3 takes a contiguous bf16 tensor")
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    usp_quantize_e4m3(x, out, x.numel(), inv_scale, stream)
+    return out
+
+
+def attn_forward_fp8(q8, k8, v8, q_descale, k_descale, v_descale, *, causal=True,
+                     window=0, sink_tokens=0, cu_seqlens=None, cp=1, ud=1,
+                     layout="contiguous", softmax_scale=0.0, workspace=None, stream=None
+                     ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(out bf16, lse) for rank-major e4m3 codes q8/k8/v8 (uint8 or
+    float8_e4m3fn tensors, [B,S,H,128] or packed [T,H,128]) with per-tensor
+    descales."""
+    B, S, Hq, Hkv, D, Bl = _dims(q8, k8, cu_seqlens)
+    out = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((Bl, Hq, S) if cu_seqlens is None else (Hq, S),
+                      dtype=torch.float32, device=q8.device)
+    ws, ws_n = _use_workspace(
+        workspace, usp_attn_fwd_fp8_workspace_size(Bl, S, Hq, Hkv, D, cp, ud), q8.device)
+    usp_attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, out, lse, B, S, Hq, Hkv,
+                     D, softmax_scale, causal, window, sink_tokens, cu_seqlens, cp, ud,
+                     layout, 0, ws, ws_n, stream)
+    return out, lse
 
 
 def permute(x: torch.Tensor, kind: str, layout: str = "contiguous", cp: int = 1,

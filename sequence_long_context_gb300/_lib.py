@@ -31,6 +31,10 @@ SIGNATURES = {
                                     _i, _i, _i, _u, _vp, _sz, _vp]),
     "usp_attn_bwd_qkvpacked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i,
                                     _vp, _i, _i, _i, _i, _u, _vp, _sz, _vp]),
+    "usp_attn_fwd_fp8": (_i, [_vp, _vp, _vp, _f, _f, _f, _vp, _vp, _i, _i, _i, _i, _i, _f,
+                              _i, _i, _i, _vp, _i, _i, _i, _u, _vp, _sz, _vp]),
+    "usp_attn_fwd_fp8_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "usp_quantize_e4m3": (_i, [_vp, _vp, _i64, _f, _vp]),
     "usp_permute": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "usp_status_string": (_c.c_char_p, [_i]),
     "usp_launch_count": (_u64, []),

@@ -26,7 +26,8 @@ NVCC_FLAGS = ARCH + [
     "--expt-relaxed-constexpr", "-I", INCLUDE,
 ]
 SOURCES = ["api.cu", "permute.cu", "merge.cu", "attn_simt.cu", "decode.cu",
-           "attn_fwd_tc.cu", "attn_bwd_tc.cu", "noalloc.cu", "selftest.cu"]
+           "attn_fwd_tc.cu", "attn_bwd_tc.cu", "attn_fwd_fp8.cu", "noalloc.cu",
+           "selftest.cu"]
 
 
 def _nvcc() -> str:

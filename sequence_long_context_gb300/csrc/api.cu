@@ -265,13 +265,15 @@ const char* usp_last_error_detail(void) { return g_detail; }
 
 usp_status_t usp_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return USP_ERR_CUDA;
-  int a = read_clear_fwd_tc_status(), b = read_clear_bwd_tc_status();
-  int c = read_clear_decode_status(), d = read_clear_selftest_status();
-  if (a < 0 || b < 0 || c < 0 || d < 0) return USP_ERR_CUDA;
-  if (a == USP_ERR_TIMEOUT || b == USP_ERR_TIMEOUT || c == USP_ERR_TIMEOUT ||
-      d == USP_ERR_TIMEOUT)
-    return USP_ERR_TIMEOUT;
-  if (a != 0 || b != 0 || c != 0 || d != 0) return USP_ERR_CUDA;
+  const int words[5] = {read_clear_fwd_tc_status(), read_clear_bwd_tc_status(),
+                        read_clear_decode_status(), read_clear_selftest_status(),
+                        read_clear_fwd_fp8_status()};
+  for (int w : words)
+    if (w < 0) return USP_ERR_CUDA;
+  for (int w : words)
+    if (w == USP_ERR_TIMEOUT) return USP_ERR_TIMEOUT;
+  for (int w : words)
+    if (w != 0) return USP_ERR_CUDA;
   return USP_OK;
 }
 
@@ -561,6 +563,96 @@ usp_status_t usp_attn_decode(const void* q, const void* k, const void* v, void* 
                       lse, st);
 }
 
+namespace {
+// fp8 forward scratch: the transposed values, then (Ulysses) the head groups
+// of the e4m3 q, k, v and of the bf16 output.
+struct Fp8Ws {
+  void *vt, *q, *k, *v, *o;
+};
+Fp8Ws carve_fwd_fp8(Carve& c, const Shape& s) {
+  Fp8Ws w{};
+  const size_t q8 = (size_t)s.B_eff() * s.S * s.Hq * s.D;
+  const size_t kv8 = (size_t)s.B_eff() * s.S * s.Hkv * s.D;
+  w.vt = c.take(kv8);
+  if (s.ud > 1) {
+    w.q = c.take(q8);
+    w.k = c.take(kv8);
+    w.v = c.take(kv8);
+    w.o = c.take(2 * q8);
+  }
+  return w;
+}
+}  // namespace
+
+size_t usp_attn_fwd_fp8_workspace_size(int B, int S, int Hq, int Hkv, int D, int cp,
+                                       int ud) {
+  if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || D < 1 || cp < 1 || ud < 1) return 0;
+  Shape s = shape_of(B, S, Hq, Hkv, D, cp, ud, 0, USP_BF16, 0);
+  Carve c(nullptr);
+  carve_fwd_fp8(c, s);
+  return c.used;
+}
+
+usp_status_t usp_attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
+                              float k_descale, float v_descale, void* out, float* lse, int B,
+                              int S, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                              int window, int sink_tokens, const int32_t* cu_seqlens,
+                              int cp_size, int ulysses_degree, usp_layout_t layout,
+                              unsigned flags, void* workspace, size_t workspace_bytes,
+                              usp_stream_t stream) {
+  (void)flags;
+  Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, USP_BF16,
+                     cu_seqlens != nullptr);
+  usp_status_t r = validate(s, window, sink_tokens);
+  if (r != USP_OK) return r;
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !(v_descale > 0.f) ||
+      !std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
+    return USP_ERR_INVALID_ARG;
+  if (S > 0 && (!q || !k || !v || !out || !lse)) return USP_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, out, lse, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return USP_ERR_ALIGNMENT;
+  AttnParams P = make_params(s, softmax_scale, causal, window, sink_tokens, cu_seqlens);
+  if (!fwd_fp8_supported(P)) return USP_ERR_UNSUPPORTED;
+  if (s.B_eff() == 0 || S == 0) return USP_OK;
+  Carve c(workspace);
+  Fp8Ws w = carve_fwd_fp8(c, s);
+  if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the codes' scales: s = scale * <q, k> of the real values
+  P.scale *= q_descale * k_descale;
+  P.scale_log2 *= q_descale * k_descale;
+  const void* vsrc = v;
+  if (s.ud > 1) {
+    const int B_eff = s.B_eff();
+    if ((r = launch_ulysses(q, w.q, B_eff, S, Hq * D, s.ud, 1, st)) != USP_OK) return r;
+    if ((r = launch_ulysses(k, w.k, B_eff, S, Hkv * D, s.ud, 1, st)) != USP_OK) return r;
+    if ((r = launch_ulysses(v, w.v, B_eff, S, Hkv * D, s.ud, 1, st)) != USP_OK) return r;
+    P.q = w.q;
+    P.k = w.k;
+    P.o = w.o;
+    vsrc = w.v;
+  } else {
+    P.q = q;
+    P.k = k;
+    P.o = out;
+  }
+  if ((r = launch_v_transpose(vsrc, w.vt, P.Bt, S, P.Hkv, st)) != USP_OK) return r;
+  P.v = w.vt;
+  P.lse = lse;
+  if ((r = launch_fwd_fp8(P, v_descale, st)) != USP_OK) return r;
+  if (s.ud > 1) r = launch_ulysses(w.o, out, s.B_eff(), S, Hq * D * 2, s.ud, 0, st);
+  return r;
+}
+
+usp_status_t usp_quantize_e4m3(const void* x, void* out, int64_t n, float inv_scale,
+                               usp_stream_t stream) {
+  if (n < 0 || !std::isfinite(inv_scale)) return USP_ERR_INVALID_ARG;
+  if (n > 0 && (!x || !out)) return USP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return USP_ERR_ALIGNMENT;
+  return launch_quantize_e4m3(x, out, n, inv_scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
 usp_status_t usp_merge_partials(const float* o_parts, const float* lse_parts,
                                 int n, int64_t rows, int D, int tree_order,
                                 void* o_out, usp_dtype_t out_dtype,
@@ -584,7 +676,7 @@ usp_status_t usp_permute(const void* src, void* dst, usp_permute_kind_t kind,
                          usp_stream_t stream) {
   if (B < 0 || S < 0 || H <= 0 || D <= 0 || cp_size < 1 || ulysses_degree < 1)
     return USP_ERR_INVALID_ARG;
-  if (elem_bytes != 2 && elem_bytes != 4) return USP_ERR_INVALID_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return USP_ERR_INVALID_ARG;
   if (layout < USP_LAYOUT_CONTIGUOUS || layout > USP_LAYOUT_STRIPE)
     return USP_ERR_INVALID_ARG;
   long long row = (long long)H * D * elem_bytes;

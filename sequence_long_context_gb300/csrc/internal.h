@@ -62,6 +62,15 @@ usp_status_t launch_fwd_tc(const AttnParams& P, cudaStream_t st);
 
 int read_clear_fwd_tc_status();  // -1 on a CUDA error
 
+// attn_fwd_fp8.cu (tcgen05 tensor-core forward, e4m3 q/k/v, D = 128)
+bool fwd_fp8_supported(const AttnParams& P);
+usp_status_t launch_fwd_fp8(const AttnParams& P, float v_descale, cudaStream_t st);
+usp_status_t launch_v_transpose(const void* v, void* vt, int Bt, int S, int H,
+                                cudaStream_t st);
+usp_status_t launch_quantize_e4m3(const void* x, void* out, long long n, float inv_scale,
+                                  cudaStream_t st);
+int read_clear_fwd_fp8_status();  // -1 on a CUDA error
+
 // attn_bwd_tc.cu (tcgen05 tensor-core backward, bf16)
 usp_status_t launch_decode_split(const void* q, const void* k, const void* v, float* o_part,
                                  float* lse_part, int B, int Tq, int S, int Hq, int Hkv, int D,

@@ -86,6 +86,8 @@ def test_fwd_rejects_before_launch(lib, over, code):
 def test_permute_and_merge_reject(lib):
     # elem_bytes, layout, divisibility, alignment
     assert lib.usp_permute(FAKE, FAKE, 0, 1, 1, 100, 2, 64, 4, 1, 3, None) == 1
+    # 1-byte codes: the row (H*D bytes) must still be a multiple of 16
+    assert lib.usp_permute(FAKE, FAKE, 0, 1, 1, 128, 1, 8, 4, 1, 1, None) == 1
     assert lib.usp_permute(FAKE, FAKE, 0, 9, 1, 128, 2, 64, 4, 1, 2, None) == 1
     assert lib.usp_permute(FAKE, FAKE, 0, 1, 1, 100, 2, 64, 4, 1, 2, None) == 1
     assert lib.usp_permute(FAKE + 4, FAKE, 0, 1, 1, 128, 2, 64, 4, 1, 2, None) == 3
@@ -204,3 +206,41 @@ def test_python_saved_exchange_needs_the_workspace():
     k = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         usp.attn_backward(q, k, k, q, None, q, cp=2, ud=2, saved_exchange=True)
+
+
+def fp8_fwd(lib, **over):
+    # zigzag, ring of 2, S = 1024: 256-token chunks, the smallest the kernel takes
+    a = dict(q=FAKE, k=FAKE, v=FAKE, qd=1.0, kd=1.0, vd=1.0, out=FAKE, lse=FAKE, B=1, S=1024,
+             Hq=4, Hkv=2, D=128, scale=0.0, causal=1, window=0, sink=0, cu=None, cp=2, ud=1,
+             layout=1, flags=0, ws=None, wsb=0, stream=None)
+    a.update(over)
+    return lib.usp_attn_fwd_fp8(a["q"], a["k"], a["v"], a["qd"], a["kd"], a["vd"], a["out"],
+                                a["lse"], a["B"], a["S"], a["Hq"], a["Hkv"], a["D"], a["scale"],
+                                a["causal"], a["window"], a["sink"], a["cu"], a["cp"], a["ud"],
+                                a["layout"], a["flags"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(), 4),                    # the V^T scratch is always needed
+    (dict(D=64), 2),                # head dim 128 only
+    (dict(qd=0.0), 1), (dict(vd=-1.0), 1), (dict(kd=float("inf")), 1),
+    (dict(q=FAKE + 8), 3),
+    (dict(v=None), 1),
+    (dict(cp=4), 2),                # 128-token chunks are below the 256-token pair
+    (dict(Hq=3), 1),
+])
+def test_fp8_forward_rejects_before_launch(lib, over, code):
+    assert fp8_fwd(lib, **over) == code
+
+
+def test_fp8_workspace_and_quantize_checks(lib):
+    # V^T always; with Ulysses also the e4m3 head groups and the bf16 output
+    assert usp.usp_attn_fwd_fp8_workspace_size(2, 1024, 8, 2, 128, 2, 1) == 2 * 1024 * 2 * 128
+    assert usp.usp_attn_fwd_fp8_workspace_size(2, 1024, 8, 2, 128, 2, 2) == \
+        2 * 1024 * 128 * (2 + 8 + 2 + 2 + 2 * 8)
+    assert usp.usp_attn_fwd_fp8_workspace_size(-1, 1024, 8, 2, 128, 2, 1) == 0
+    assert lib.usp_quantize_e4m3(FAKE, FAKE, -1, 1.0, None) == 1
+    assert lib.usp_quantize_e4m3(None, FAKE, 16, 1.0, None) == 1
+    assert lib.usp_quantize_e4m3(FAKE, FAKE, 16, float("inf"), None) == 1
+    assert lib.usp_quantize_e4m3(FAKE + 4, FAKE, 16, 1.0, None) == 3
+    assert lib.usp_quantize_e4m3(FAKE, FAKE, 0, 1.0, None) == 0  # nothing to do
