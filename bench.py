@@ -33,6 +33,8 @@ METRIC = ("causal attn TFLOP/s (useful FLOPs) & % of GB300 BF16 dense peak, "
           "S=8K–128K")
 DEFAULT_WORKLOAD = "usp_ud2_ring4_s8k"
 DEFAULT_DECODE = "decode_gqa_b8_s128k_cp8"
+# the e4m3 forward is reported on the shapes of the S = 32K zigzag workload
+DEFAULT_FP8 = "sweep_zigzag_cp8_s32k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
@@ -42,7 +44,7 @@ KERNEL_SOURCES = {
     "attn_bwd_dkdv_simt": "attn_simt.cu", "attn_bwd_preprocess": "attn_simt.cu",
     "permute_layout": "permute.cu", "permute_ulysses": "permute.cu",
     "merge_linear": "merge.cu", "merge_tree": "merge.cu",
-    "attn_decode_split": "decode.cu",
+    "attn_decode_split": "decode.cu", "attn_fwd_fp8": "attn_fwd_fp8.cu",
 }
 
 
@@ -56,6 +58,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -453,6 +456,56 @@ def main():
         except Exception as e:  # report, do not hide
             decode_res = {"error": repr(e)}
 
+    # fp8 (E4M3) forward: the inputs are quantized once, outside the timed
+    # region; the forward (V transpose + attention) runs on resident codes.
+    # Tensor-bound: reported against the measured bf16 peak times the
+    # nominal e4m3 / bf16 rate ratio (4.5 / 2.25 PFLOP/s dense).
+    fp8_res = None
+    if not args.no_fp8:
+        try:
+            fw = WORKLOADS[DEFAULT_FP8]
+            fx = make_inputs(fw, seed=args.seed, device=str(dev))
+            codes = []
+            for n in "qkv":
+                t = usp.permute(fx[n], "extract", fw.layout, fw.cp)
+                inv = 256.0 / float(t.float().abs().max())
+                codes.append((usp.quantize_e4m3(t, inv), 1.0 / inv))
+            del fx
+            (q8, qd), (k8, kd), (v8, vd) = codes
+            fws = torch.empty(usp.usp_attn_fwd_fp8_workspace_size(
+                fw.B, fw.S, fw.Hq, fw.Hkv, fw.D, fw.cp, fw.ud), dtype=torch.uint8, device=dev)
+            ffn = lambda: usp.attn_forward_fp8(  # noqa: E731
+                q8, k8, v8, qd, kd, vd, causal=fw.causal, window=fw.window,
+                sink_tokens=fw.sink_tokens, cp=fw.cp, ud=fw.ud, layout=fw.layout,
+                workspace=fws)
+            for _ in range(3):
+                ffn()
+            usp.usp_profile_enable(True)
+            fms = timed(ffn, 10)
+            usp.usp_profile_enable(False)
+            fk = usp.usp_profile_read()
+            ff = flops.attention_flops(fw)["fwd"]
+            fp8_peak = 2.0 * pk["bf16_tflops"]
+            att = fk.get("attn_fwd_fp8")
+            att_ms = att[1] / att[0] if att else None
+            fp8_res = {
+                "workload": fw.name, "B": fw.B, "S": fw.S, "Hq": fw.Hq, "Hkv": fw.Hkv,
+                "D": fw.D, "cp": fw.cp, "layout": fw.layout, "causal": fw.causal,
+                "dtype": "e4m3", "forward_ms": fms,
+                "forward_tflops": ff / (fms * 1e-3) / 1e12,
+                "kernel_ms": att_ms,
+                "roofline": {"kernel": "attn_fwd_fp8", "bound": "tensor",
+                             "achieved": ff / (att_ms * 1e-3) / 1e12 if att_ms else None,
+                             "peak": fp8_peak, "unit": "TFLOP/s",
+                             "frac": ff / (att_ms * 1e-3) / 1e12 / fp8_peak if att_ms else None,
+                             "peak_source": "measured bf16_tflops x 2 (nominal e4m3/bf16 ratio)",
+                             "traffic": traffic_for("attn_fwd_fp8", fw.name)},
+                "kernels": {k: {"launches_per_step": v[0] / 10, "avg_ms": v[1] / v[0]}
+                            for k, v in fk.items()}}
+            del codes, q8, k8, v8, fws
+        except Exception as e:  # report, do not hide
+            fp8_res = {"error": repr(e)}
+
     # end to end: every step uploads its inputs from pinned host memory and
     # reads its results back into pinned host memory. The copies run on their
     # own streams, double-buffered: step i+1's upload and step i-1's readback
@@ -524,7 +577,7 @@ def main():
         "config": workload_config(w, F["total"], world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches * args.steps), "clocks": clocks,
-        "kernels": kernels, "merge": merge_res, "decode": decode_res,
+        "kernels": kernels, "merge": merge_res, "decode": decode_res, "fp8": fp8_res,
     }
     if rank == 0:
         print(json.dumps(line))
