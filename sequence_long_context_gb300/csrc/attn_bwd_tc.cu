@@ -701,11 +701,24 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   }
   AttnParams Pk = P;
   Pk.status = status;
-  // L2 batches: enough key tiles for about one and a half waves of CTAs
+  // L2 batches of units (KV head, batch), heaviest CTAs first inside each.
+  // Contiguous and zigzag: about 6.5 waves of CTAs per batch. Their CTAs walk
+  // the query shards in ring order, so a batch touches a moving window of
+  // query tiles, and wide batches spread the CTAs that reach the same
+  // (popular, late) query tiles over more heads: at S=8K with 64 key tiles
+  // per head, 16 heads per batch ran the backward 7 % faster than 4, and
+  // the S=32K ring 5 % faster with 4 KV groups than with 1. Stripe: about
+  // 1.5 waves, since every key tile visits nearly every query tile of its
+  // head and wider batches overflow L2 (S=32K: 19.4 ms with 1 group, 25.2
+  // with 8). Packed sequences: one batch, since a key tile only meets the
+  // query tiles of its own sequence.
   {
     const int ntiles = P.S / kTile;
-    const int per = (3 * sm_count() / 2 + ntiles - 1) / ntiles;
-    Pk.unit_batch = per < P.Hkv * P.Bt ? per : P.Hkv * P.Bt;
+    const int units = P.Hkv * P.Bt;
+    const int waves2 = P.layout == kStripe ? 3 : 13;  // twice the waves per batch
+    int per = (waves2 * sm_count() / 2 + ntiles - 1) / ntiles;
+    if (P.cu != nullptr) per = units;
+    Pk.unit_batch = per < units ? per : units;
   }
   const int smem = BSmem<D>::kAlloc;
   static bool attr_set = false;

@@ -642,9 +642,11 @@ usp_status_t launch_fwd_fp8(const AttnParams& P, float v_descale, cudaStream_t s
   }
   AttnParams Pk = P;
   Pk.status = status;
+  // L2 batches as in the bf16 forward: about eight waves of CTAs, in whole
+  // GQA groups
   {
     const int npairs = P.S / (2 * kBM);
-    int per = (2 * sm_count() + npairs - 1) / npairs;
+    int per = (8 * sm_count() + npairs - 1) / npairs;
     per = (per + P.G - 1) / P.G * P.G;
     Pk.unit_batch = per < P.Hq * P.Bt ? per : P.Hq * P.Bt;
   }
