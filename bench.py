@@ -515,7 +515,7 @@ def main():
             cs.wait_stream(down)
 
         e2e_run(4)
-        n_e2e = max(3, min(args.steps, 10))
+        n_e2e = max(3, min(2 * args.steps, 20))
         ems = timed(lambda: e2e_run(n_e2e), 1) / n_e2e
         d2h = sum(t.numel() * t.element_size() for t in outs_host[0])
         e2e = {"value": F["total"] * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
