@@ -218,6 +218,22 @@ def workload_config(w, total_flop: float, world: int) -> dict:
             "l2": "no flush: step inputs larger than L2"}
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (the job ends when its last rank does)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_rank_step: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return flop_per_rank_step * world / (ms * 1e-3) / 1e12
+
+
 def run_reference(args):
     """The oracle timed on the host cores, as the reference arm."""
     import numpy as np  # noqa: F401
@@ -316,12 +332,7 @@ def main():
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        ms = a.elapsed_time(b) / n
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(a.elapsed_time(b) / n, world, dev)
 
     for _ in range(args.warmup):
         step(x)
@@ -518,7 +529,7 @@ def main():
         n_e2e = max(3, min(2 * args.steps, 20))
         ems = timed(lambda: e2e_run(n_e2e), 1) / n_e2e
         d2h = sum(t.numel() * t.element_size() for t in outs_host[0])
-        e2e = {"value": F["total"] * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_tflops(F["total"], world, ems), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
                "steps": n_e2e, "copies": "double-buffered on separate H2D/D2H streams"}
 
@@ -578,7 +589,7 @@ def main():
         cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                "sample": desc, "seconds": dt}
 
-    value = F["total"] * world / (ms * 1e-3) / 1e12
+    value = job_tflops(F["total"], world, ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
