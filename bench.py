@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-gate", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -270,6 +271,68 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def make_step(usp, w, x, cu_dev):
+    """One training pass of workload w over the natural-order inputs `inp`:
+    extract, forward, backward (reusing the forward's Ulysses exchange from
+    the shared workspace), restore. Returns the natural-order results."""
+    kw = dict(causal=w.causal, window=w.window, sink_tokens=w.sink_tokens,
+              cu_seqlens=cu_dev, cp=w.cp, ud=w.ud, layout=w.layout)
+    # one workspace for the forward and the backward of every step: the
+    # backward reads the forward's head-sharded q, k, v, out from it instead
+    # of exchanging them again
+    ws = usp.attn_workspace(x["q"], x["k"], cu_seqlens=cu_dev, cp=w.cp, ud=w.ud)
+
+    def step(inp):
+        qp, kp, vp = (usp.permute(inp[n], "extract", w.layout, w.cp) for n in "qkv")
+        out, lse = usp.attn_forward(qp, kp, vp, workspace=ws, **kw)
+        res = [out]
+        if w.backward:
+            dop = usp.permute(inp["dout"], "extract", w.layout, w.cp)
+            res += list(usp.attn_backward(qp, kp, vp, out, lse, dop, workspace=ws,
+                                          saved_exchange=True, **kw))
+        return [usp.permute(r, "restore", w.layout, w.cp) for r in res]
+
+    return step
+
+
+def gate_point(usp, flops, torch, name, dev, seed, steps, warmup, pk, timed):
+    """Forward and backward tensor-core kernels of one zigzag sweep point,
+    each kernel's average CUDA-event time over `steps` training steps and its
+    useful TFLOP/s against the bf16 peak (burst when the timed region is
+    short, sustained beyond 2 s; both fractions are reported)."""
+    from sequence_long_context_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[name]
+    x = make_inputs(w, seed=seed, device=str(dev))
+    F = flops.attention_flops(w)
+    step = make_step(usp, w, x, None)
+    for _ in range(warmup):
+        step(x)
+    torch.cuda.synchronize()
+    usp.usp_profile_enable(True)
+    ms = timed(lambda: step(x), steps)
+    usp.usp_profile_enable(False)
+    ks = usp.usp_profile_read()
+    region_s = ms * steps / 1e3
+    peak = pk["bf16_tflops_sustained"] if region_s > 2.0 else pk["bf16_tflops"]
+    res = {"workload": name, "S": w.S, "step_ms": ms, "steps": steps,
+           "step_tflops": F["total"] / (ms * 1e-3) / 1e12,
+           "peak_used": "bf16_tflops_sustained" if region_s > 2.0 else "bf16_tflops"}
+    for part, kname, work in (("fwd", "attn_fwd_tc", F["fwd"]), ("bwd", "attn_bwd_tc", F["bwd"])):
+        n, tot = ks.get(kname, (0, 0.0))
+        if not n:
+            res[part] = {"error": f"{kname} did not run"}
+            continue
+        avg = tot / n
+        ach = work / (avg * 1e-3) / 1e12
+        res[part] = {"kernel": kname, "avg_ms": avg, "useful_tflop": work / 1e12,
+                     "achieved": ach, "frac": ach / peak,
+                     "frac_of_burst": ach / pk["bf16_tflops"],
+                     "frac_of_sustained": ach / pk["bf16_tflops_sustained"]}
+    del x, step
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -301,23 +364,8 @@ def main():
     cu_dev = cu.to(dev) if cu is not None else None
     F = flops.attention_flops(w, cu.tolist() if cu is not None else None)
     names = ["q", "k", "v"] + (["dout"] if w.backward else [])
-    kw = dict(causal=w.causal, window=w.window, sink_tokens=w.sink_tokens,
-              cu_seqlens=cu_dev, cp=w.cp, ud=w.ud, layout=w.layout)
 
-    # one workspace for the forward and the backward of every step: the
-    # backward reads the forward's head-sharded q, k, v, out from it instead
-    # of exchanging them again
-    ws = usp.attn_workspace(x["q"], x["k"], cu_seqlens=cu_dev, cp=w.cp, ud=w.ud)
-
-    def step(inp):
-        qp, kp, vp = (usp.permute(inp[n], "extract", w.layout, w.cp) for n in "qkv")
-        out, lse = usp.attn_forward(qp, kp, vp, workspace=ws, **kw)
-        res = [out]
-        if w.backward:
-            dop = usp.permute(inp["dout"], "extract", w.layout, w.cp)
-            res += list(usp.attn_backward(qp, kp, vp, out, lse, dop, workspace=ws,
-                                          saved_exchange=True, **kw))
-        return [usp.permute(r, "restore", w.layout, w.cp) for r in res]
+    step = make_step(usp, w, x, cu_dev)
 
     def timed(fn, n):
         if world > 1:
@@ -388,10 +436,12 @@ def main():
     kv_bytes = (1 if w.varlen else w.B) * w.S * w.Hkv * w.D * elem
     # tensor bytes moved per step by each permute family (each byte is read
     # once and written once): extract q,k,v(,dO), restore O(,dQ,dK,dV); the
-    # Ulysses exchange inside the attention calls when ud > 1.
+    # Ulysses exchange inside the attention calls when ud > 1: q, k, v in and
+    # out back in the forward; the backward reuses the forward's exchange
+    # (saved_exchange) and moves dO in and dQ, dK, dV back.
     if w.backward:
         moved = {"permute_layout": 4 * q_bytes + 4 * kv_bytes,
-                 "permute_ulysses": 6 * q_bytes + 6 * kv_bytes}
+                 "permute_ulysses": 4 * q_bytes + 4 * kv_bytes}
     else:
         moved = {"permute_layout": 2 * q_bytes + 2 * kv_bytes,
                  "permute_ulysses": 2 * q_bytes + 2 * kv_bytes}
@@ -466,6 +516,18 @@ def main():
             del dx
         except Exception as e:  # report, do not hide
             decode_res = {"error": repr(e)}
+
+    # the throughput gate: the zigzag causal sweep (B=1, 32/8 heads, D=128,
+    # cp=8) at S = 32K, and the end of the metric's range at S = 128K
+    gate = None
+    if not args.no_gate:
+        gate = {"targets": {"fwd_frac": 0.60, "bwd_frac": 0.45, "at": "sweep_zigzag_cp8_s32k"}}
+        for gname, gsteps in (("sweep_zigzag_cp8_s32k", 10), ("sweep_zigzag_cp8_s128k", 2)):
+            try:
+                gate[gname] = gate_point(usp, flops, torch, gname, dev, args.seed, gsteps, 3,
+                                         peaks()[0], timed)
+            except Exception as e:  # report, do not hide
+                gate[gname] = {"error": repr(e)}
 
     # end to end: every step uploads its inputs from pinned host memory and
     # reads its results back into pinned host memory. The copies run on their
@@ -598,7 +660,8 @@ def main():
         "config": workload_config(w, F["total"], world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches * args.steps), "clocks": clocks,
-        "kernels": kernels, "merge": merge_res, "decode": decode_res, "fp8": fp8_res,
+        "gate": gate, "kernels": kernels, "merge": merge_res, "decode": decode_res,
+        "fp8": fp8_res,
     }
     if rank == 0:
         print(json.dumps(line))

@@ -240,7 +240,10 @@ def attn_bwd_sampled(q, k, v, dout, scale: float, b: int, g: int,
     Returns (dq [G, nq, D] for q_rows of every query head of KV group g,
     dk [nk, D], dv [nk, D] for k_rows of KV head g), batch b (packed: b=0).
     Uses the identity sum_j P_ij dP_ij = <dO_i, O_i> (the P row sums to one),
-    with O and LSE from this module's own forward of the group's heads.
+    with O and LSE from this module's own forward of the group's heads. That
+    forward covers only the query rows the result needs: q_rows and every
+    query that sees one of k_rows (the visibility rule decides which); the
+    other rows enter no sampled gradient.
     """
     packed = cu_seqlens is not None
     sel = (lambda t: t) if packed else (lambda t: t[b])
@@ -257,26 +260,41 @@ def attn_bwd_sampled(q, k, v, dout, scale: float, b: int, g: int,
     # are independent and run on threads (NumPy releases the GIL).
     O = np.zeros((G, S, D))
     L = np.zeros((G, S))
+    q_rows = [int(r) for r in q_rows]
+    k_rows = [int(r) for r in k_rows]
+    # per segment: the local query positions whose O and LSE are needed
+    need = []
+    for (a, e) in segs:
+        pos = np.arange(e - a)
+        nd = np.zeros(e - a, dtype=bool)
+        nd[[r - a for r in q_rows if a <= r < e]] = True
+        ks = np.array([j - a for j in k_rows if a <= j < e], dtype=np.int64)
+        if ks.size:
+            nd |= visibility(pos, ks, causal, window, sink_tokens).any(axis=1)
+        need.append(nd)
 
     def head_fwd(hi):
-        for (a, e) in segs:
+        for (a, e), nd in zip(segs, need):
             pos = np.arange(e - a)
             for r0 in range(0, e - a, block):
                 r1 = min(e - a, r0 + block)
-                kend = r1 if causal else e - a
-                vis = visibility(pos[r0:r1], pos[:kend], causal, window,
+                rr = r0 + np.nonzero(nd[r0:r1])[0]
+                if rr.size == 0:
+                    continue
+                # with causal, keys past the block's last needed query are
+                # never visible to it; cutting them only saves time
+                kend = int(rr[-1]) + 1 if causal else e - a
+                vis = visibility(pos[rr], pos[:kend], causal, window,
                                  sink_tokens)
-                o, lse = softmax_rows(qb[a + r0:a + r1, hi], kk[a:a + kend],
+                o, lse = softmax_rows(qb[a + rr, hi], kk[a:a + kend],
                                       vv[a:a + kend], vis, scale)
-                O[hi, a + r0:a + r1] = o
-                L[hi, a + r0:a + r1] = lse
+                O[hi, a + rr] = o
+                L[hi, a + rr] = lse
 
     from concurrent.futures import ThreadPoolExecutor
     with ThreadPoolExecutor(max_workers=G) as ex:
         list(ex.map(head_fwd, range(G)))
     delta = np.einsum("hsd,shd->hs", O, dob)
-    q_rows = [int(r) for r in q_rows]
-    k_rows = [int(r) for r in k_rows]
     dq = np.zeros((G, len(q_rows), D))
     for n, r in enumerate(q_rows):
         si = int(np.searchsorted(starts, r, side="right") - 1)

@@ -20,9 +20,12 @@ from tests._gpu import TOL, device, lse_to_natural, rel_fro, run_backward, run_f
 
 pytestmark = pytest.mark.gpu
 
+# the five problem statements, the sliding-window training step, and the
+# zigzag sweep points that carry the throughput gate (S = 32K) and the end of
+# the measured range (S = 128K: a 2 GiB fp32 dQ accumulator)
 CONFIGS = ["usp_ud2_ring4_s8k", "gqa_stripe_cp8_s32k", "swa_w1000_cp8_s8k",
            "swa_w1000_sink4_cp8_s8k", "swa_w1000_sink4_cp8_s8k_train",
-           "varlen_zigzag_cp8_t128k"]
+           "varlen_zigzag_cp8_t128k", "sweep_zigzag_cp8_s32k", "sweep_zigzag_cp8_s128k"]
 
 
 def sample_positions(w, rng, n=40):
@@ -65,7 +68,16 @@ def test_full_config(name):
     if grads is None:
         return
     b = batches[-1]
-    keys = sample_positions(w, rng, 24)
+    if w.S >= 131072:
+        # at S = 128K the dK/dV rows are keys of the last 4096 positions: the
+        # oracle needs the forward of every query that sees a sampled key,
+        # and these are seen by at most 4096 queries each (the dQ rows above
+        # still span the whole sequence)
+        lo = w.S - 4096
+        keys = sorted({lo, lo + 1, w.S - 129, w.S - 128, w.S - 1}
+                      | set(rng.choice(np.arange(lo, w.S), 19, replace=False).tolist()))
+    else:
+        keys = sample_positions(w, rng, 24)
     dq_ref, dk_ref, dv_ref = attention.attn_bwd_sampled(
         xc["q"], xc["k"], xc["v"], xc["dout"], w.scale, b, g, rows, keys,
         w.causal, w.window, w.sink_tokens, cu_seqlens=cu)

@@ -88,6 +88,43 @@ def test_merge_bf16_output():
     np.testing.assert_allclose(oo.cpu().double().numpy(), O, atol=2e-2)
 
 
+def _merge_check_all_rows(oo, ll, o, lse, tree, rtol_o):
+    """Every output row against the oracle, in row chunks (rows are independent)."""
+    n, rows = lse.shape
+    fn = merge.merge_tree if tree else merge.merge_linear
+    step = 1 << 15
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        parts = [(np.nan_to_num(o[i, r0:r1].double().numpy()), lse[i, r0:r1].double().numpy())
+                 for i in range(n)]
+        O, L = fn(parts)
+        got_o = oo[r0:r1].double().numpy()
+        got_l = ll[r0:r1].double().numpy()
+        fin = np.isfinite(L)
+        assert np.array_equal(np.isneginf(got_l), ~fin), r0
+        np.testing.assert_allclose(got_l[fin], L[fin], rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(got_o[fin], O[fin], rtol=rtol_o, atol=1e-5)
+        assert np.all(got_o[~fin] == 0), r0
+
+
+# The benchmark's merge workload (n partials of B*S*Hq = 524288 rows, D = 128)
+# at full size: every row is compared, so every iteration of the kernels'
+# grid-stride loops (a persistent one-wave grid) and the last, partial pass
+# are covered. n = 17 runs the kernels for more than eight partials.
+@pytest.mark.parametrize("n,rows", [(4, 524288), (8, 524288), (17, 131072 + 77)])
+@pytest.mark.parametrize("tree", [False, True])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_merge_full_size(n, rows, tree, out_dtype):
+    dev = device()
+    o, lse = _partials(n, rows, 128, 1000 + n)
+    oo, ll = usp.merge_partials(o.to(dev), lse.to(dev), tree_order=tree, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    # bf16 output: the fp32 result rounded once to nearest, which is within
+    # one bf16 ulp (2^-7 relative) even after the fp32 arithmetic
+    _merge_check_all_rows(oo.cpu(), ll.cpu(), o, lse, tree,
+                          2.0 ** -7 if out_dtype == torch.bfloat16 else 1e-5)
+
+
 def test_merge_empty_rows_ok():
     dev = device()
     o = torch.zeros(3, 0, 128, device=dev)

@@ -388,3 +388,25 @@ def test_sampled_bwd_matches_full(varlen):
     np.testing.assert_allclose(sq, np.transpose(sel(dq)[rows][:, 3:6], (1, 0, 2)), atol=1e-12)
     np.testing.assert_allclose(sk, sel(dk)[keys, 1], atol=1e-12)
     np.testing.assert_allclose(sv, sel(dv)[keys, 1], atol=1e-12)
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_sampled_bwd_late_keys_matches_full(varlen):
+    # keys late in their sequences are seen by few queries, so the sampled
+    # backward computes the forward of only those rows (and of the dq rows):
+    # the skipped rows must not matter
+    S, Hq, Hkv, D = 48, 4, 2, 8
+    cu = [0, 20, 21, 48] if varlen else None
+    if varlen:
+        q, k, v, do = rnd((S, Hq, D), 80), rnd((S, Hkv, D), 81), rnd((S, Hkv, D), 82), rnd((S, Hq, D), 83)
+    else:
+        q, k, v, do = rnd((1, S, Hq, D), 80), rnd((1, S, Hkv, D), 81), rnd((1, S, Hkv, D), 82), rnd((1, S, Hq, D), 83)
+    for kw in (dict(causal=True), dict(causal=True, window=6, sink_tokens=1)):
+        dq, dk, dv = attention.attn_bwd(q, k, v, do, 0.35, cu_seqlens=cu, **kw)
+        rows, keys = [3, 19, 33], [17, 19, 20, 44, 47]
+        sq, sk, sv = attention.attn_bwd_sampled(q, k, v, do, 0.35, 0, 1, rows, keys,
+                                                cu_seqlens=cu, **kw)
+        sel = (lambda t: t) if varlen else (lambda t: t[0])
+        np.testing.assert_allclose(sq, np.transpose(sel(dq)[rows][:, 2:4], (1, 0, 2)), atol=1e-12)
+        np.testing.assert_allclose(sk, sel(dk)[keys, 1], atol=1e-12)
+        np.testing.assert_allclose(sv, sel(dv)[keys, 1], atol=1e-12)
