@@ -205,17 +205,26 @@ size_t usp_attn_bwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
  * takes its scratch from one fixed 64 MiB array in device memory that the
  * library declares at file scope. It calls no cudaMalloc, cudaFree or other
  * allocating routine.
- *  - Limit: a problem whose usp_attn_bwd_workspace_size (with B = 1 for
- *    packed batches) exceeds 64 MiB is rejected with USP_ERR_WORKSPACE
- *    before anything is launched (usp_last_error_detail() says why).
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *  - Arguments are checked first, exactly as usp_attn_bwd checks them
+ *    (USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, ... before anything else).
+ *  - Limit: a problem whose backward scratch (usp_attn_bwd_workspace_size,
+ *    B = 1 for packed batches, for the kernels the call would use) exceeds
+ *    64 MiB is rejected with USP_ERR_WORKSPACE before anything is launched
+ *    (usp_last_error_detail() says why).
+ *  - Set-up: the first call on each device (and the first after the
+ *    device's context has been reset) looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it. That
+ *    lookup is also when the 64 MiB are taken from the device: the array
+ *    belongs to a module the CUDA runtime loads on first use (its default,
+ *    lazy module loading), and it stays reserved until the process exits.
+ *    So make one call on each device before handing the rest of its memory
+ *    to a pool and before any stream capture; a call with S = 0 and
+ *    otherwise valid sizes (the tensor pointers may then be NULL) does only
+ *    this set-up and launches nothing.
  *  - Every call shares the one array, which keeps the last call's contents;
  *    what must start at zero is cleared on the device at the start of each
  *    call. Calls that overlap on the GPU (e.g. on two streams) race on the
  *    array and give wrong results; serialise them.
- *  - Every GPU that loads the library holds the 64 MiB until process exit.
  * Errors: as usp_attn_bwd, plus USP_ERR_WORKSPACE for the size limit.
  */
 usp_status_t usp_attn_bwd_noalloc(const void *q, const void *k, const void *v,

@@ -13,6 +13,14 @@
 // the GPU (for example on two streams) race on it. Its contents persist
 // between calls; everything the kernels need zeroed (the dQ accumulator) is
 // cleared on the device at the start of every call.
+//
+// When the array takes device memory: it belongs to this file's module,
+// which the CUDA runtime loads on a device when something first needs it
+// there. With the runtime's default lazy module loading that is the first
+// usp_attn_bwd_noalloc call on the device (its cudaGetSymbolAddress), so
+// the 64 MiB are reserved then, and stay until the process exits.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -23,16 +31,49 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 constexpr int kMaxDevices = 256;
 
-// Every GPU that loads this library holds these 64 MiB until the process
-// exits. In host code this name is only a stand-in for the symbol; the
-// device address comes from cudaGetSymbolAddress.
+// In host code this name is only a stand-in for the symbol; the device
+// address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct DeviceScratch {
+  void* addr;
+  unsigned long long ctx_id;  // context the address belongs to
+};
+DeviceScratch g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up
-// once per device (with that device current) and cached.
+// Unique id of the calling thread's current context (0 if there is none or
+// the driver cannot say). A device reset destroys the context and the next
+// one gets a new id, so an address looked up before the reset is not reused.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device. It is looked
+// up (with that device current) on the first call on each device and again
+// whenever the device's context has changed since (after a device reset);
+// otherwise the cached address is returned.
 usp_status_t scratch_on_current_device(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -40,13 +81,17 @@ usp_status_t scratch_on_current_device(void** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return fail_cuda_msg("usp_attn_bwd_noalloc", "device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  DeviceScratch& s = g_scratch[dev];
+  const unsigned long long ctx = current_context_id();
+  if (s.addr == nullptr || ctx == 0 || ctx != s.ctx_id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return fail_cuda("cudaGetSymbolAddress(scratch)", e);
-    g_scratch_addr[dev] = p;
+    s.addr = p;
+    // the lookup has made the device's context current if it was not yet
+    s.ctx_id = ctx != 0 ? ctx : current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = s.addr;
   return USP_OK;
 }
 
@@ -72,22 +117,24 @@ usp_status_t usp_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                      "forward's workspace, which this call does not take");
     return USP_ERR_INVALID_ARG;
   }
-  // Packed batches keep one leading batch row in their tensors.
-  const int b_tensor = cu_seqlens != nullptr ? 1 : B;
-  const size_t need = usp_attn_bwd_workspace_size(
-      b_tensor, S, Hq, Hkv, D, cp_size, ulysses_degree, dtype, flags);
-  if (need > kNoAllocScratchBytes) {
-    set_error_detail("usp_attn_bwd_noalloc: problem needs more scratch than "
-                     "the fixed 64 MiB array holds");
-    return USP_ERR_WORKSPACE;
-  }
+  // Argument check first, without a workspace: usp_attn_bwd validates every
+  // argument and then refuses the missing workspace before it launches
+  // anything, or returns USP_OK at once for an empty problem.
+  const usp_status_t dry = usp_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D,
+                                        softmax_scale, causal, window, sink_tokens, cu_seqlens,
+                                        cp_size, ulysses_degree, layout, dtype, flags, nullptr,
+                                        0, stream);
+  if (dry != USP_OK && dry != USP_ERR_WORKSPACE) return dry;
   void* scratch = nullptr;
   usp_status_t r = scratch_on_current_device(&scratch);
-  if (r != USP_OK) return r;
-  return usp_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D,
-                      softmax_scale, causal, window, sink_tokens, cu_seqlens,
-                      cp_size, ulysses_degree, layout, dtype, flags, scratch,
-                      kNoAllocScratchBytes, stream);
+  if (r != USP_OK || dry == USP_OK) return r;  // an empty problem: set-up only
+  r = usp_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, softmax_scale,
+                   causal, window, sink_tokens, cu_seqlens, cp_size, ulysses_degree, layout,
+                   dtype, flags, scratch, kNoAllocScratchBytes, stream);
+  if (r == USP_ERR_WORKSPACE)
+    set_error_detail("usp_attn_bwd_noalloc: problem needs more scratch than "
+                     "the fixed 64 MiB array holds");
+  return r;
 }
 
 }  // extern "C"

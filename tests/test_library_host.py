@@ -244,3 +244,17 @@ def test_fp8_workspace_and_quantize_checks(lib):
     assert lib.usp_quantize_e4m3(FAKE, FAKE, 16, float("inf"), None) == 1
     assert lib.usp_quantize_e4m3(FAKE + 4, FAKE, 16, 1.0, None) == 3
     assert lib.usp_quantize_e4m3(FAKE, FAKE, 0, 1.0, None) == 0  # nothing to do
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(B=-1), 1), (dict(Hq=3), 1), (dict(D=96), 2), (dict(S=255), 1), (dict(cp=0), 1),
+    (dict(q=FAKE + 8), 3)])
+def test_noalloc_checks_arguments_first(lib, over, code):
+    # argument errors come back as usp_attn_bwd reports them, before the
+    # scratch array is looked up (no device is needed to get them)
+    a = dict(q=FAKE, B=1, S=256, Hq=4, D=64, cp=2)
+    a.update(over)
+    st = lib.usp_attn_bwd_noalloc(a["q"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  a["B"], a["S"], a["Hq"], 2, a["D"], 0.0, 1, 0, 0, None,
+                                  a["cp"], 1, 1, 0, 0, None)
+    assert st == code, lib.usp_status_string(st)
