@@ -203,6 +203,10 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       int n = 0;    // tiles with Q and dO issued
       int nq = 0;   // tiles with Q issued (n or n + 1)
       bool ok = true;
+      // packed sequences of the key tile (fixed) and of the last query tile
+      // (the next one's first guess)
+      const SegInfo sk = seg_info(P, ks);
+      int qhint = sk.first;
       // the key shard travels the ring: step s finds it on rank kappa + s
       for (int s = 0; s < P.cp && ok; ++s) {
         const int rho = (kappa + s) % P.cp;
@@ -212,7 +216,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         for (int ri = 0; ri < nr && ok; ++ri)
         for (int qt = runs[ri].begin; qt < runs[ri].end && ok; ++qt) {
           const TileSpan qsp = tile_span(P, qt * kTile);
-          const int cls = classify(P, qsp, ks);
+          const SegInfo sq = seg_info(P, qsp, qhint);
+          qhint = sq.last;
+          const int cls = classify(P, qsp, sq, ks, sk);
           if (cls == kClsEmpty) continue;
           for (int hh = 0; hh < P.G && ok; ++hh) {
             const int h = g * P.G + hh;
@@ -281,7 +287,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       constexpr uint32_t kIdKV = idesc_bf16_f32(kTile, D, 0, 1);
       const uint32_t t_s = tmem, t_dp = tmem + 128;
       const uint32_t t_dv = tmem + 256, t_dk = tmem + 256 + D;
-      const uint32_t ka = sbase + L::kK, va = sbase + L::kV, dsa = sbase + L::kDS;
+      // operand descriptors, built once and stepped by constants: K and V
+      // as K-major (S^T, dP^T) and MN-major (dQ) operands, the first Q and
+      // dO slots both ways, and the dS tile
+      const uint64_t dk_k = sdesc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t dv_k = sdesc_sw128(sbase + L::kV, 16, 1024);
+      const uint64_t dk_mn = sdesc_sw128(sbase + L::kK, L::kHalfBytes, 1024);
+      const uint64_t dq_k = sdesc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dq_mn = sdesc_sw128(sbase + L::kQ, L::kHalfBytes, 1024);
+      const uint64_t ddo_k = sdesc_sw128(sbase + L::kDO, 16, 1024);
+      const uint64_t ddo_mn = sdesc_sw128(sbase + L::kDO, L::kHalfBytes, 1024);
+      const uint64_t dds_mn = sdesc_sw128(sbase + L::kDS, L::kHalfBytes, 1024);
       bool ok = mbar_wait(bar(L::kKVFull), 0, abort_flag, P.status);
       int n = 0;
       while (ok) {
@@ -292,12 +308,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
         info[0] = e;
         mbar_arrive(bar(L::kInfoS));
-        const uint32_t qa = sbase + L::kQ + slot * L::kTileBytes;
-        const uint32_t doa = sbase + L::kDO + slot * L::kTileBytes;
+        const uint32_t slot_off = slot * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          mma_ss(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS,
+          mma_ss(t_s, sdesc_add(dk_k, off), sdesc_add(dq_k, slot_off + off), kIdS,
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kSFull));
@@ -312,8 +327,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          mma_ss(t_dp, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
-                 kIdS, kk > 0 ? 1u : 0u);
+          mma_ss(t_dp, sdesc_add(dv_k, off), sdesc_add(ddo_k, slot_off + off), kIdS,
+                 kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kDPFull));
         // dV += P^T dO as soon as P^T is in tensor memory: it runs while the
@@ -322,23 +337,21 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dv, t_s + 8 * kk + 32 * (kk >> 2),
-                 sdesc_sw128(doa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
-                 (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(t_dv, t_s + 8 * kk + 32 * (kk >> 2), sdesc_add(ddo_mn, slot_off + kk * 2048),
+                 kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
         if (!(ok = mbar_wait(bar(L::kDSFull), n & 1, abort_flag, P.status))) break;
         tc_fence_after();
         // dQ = dS K (M = queries, K dim = keys; both operands MN-major)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(t_dp, sdesc_sw128(dsa + kk * 2048, L::kHalfBytes, 1024),
-                 sdesc_sw128(ka + kk * 2048, L::kHalfBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+          mma_ss(t_dp, sdesc_add(dds_mn, kk * 2048), sdesc_add(dk_mn, kk * 2048), kIdDQ,
+                 kk > 0 ? 1u : 0u);
         mma_commit(bar(L::kDQFull));
         // dK += dS^T Q
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dk, t_s + 32 + 8 * kk + 32 * (kk >> 2),
-                 sdesc_sw128(qa + kk * 2048, L::kHalfBytes, 1024), kIdKV,
-                 (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(t_dk, t_s + 32 + 8 * kk + 32 * (kk >> 2), sdesc_add(dq_mn, slot_off + kk * 2048),
+                 kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kQEmpty + slot));
         ++n;
       }
@@ -512,7 +525,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           tma_store_4d(half ? &tm_dk : &tm_dv, smem_u32(stage + hf * L::kHalfBytes), hf * 64,
                        g, kt * kTile, bt);
         bulk_commit_group();
-        bulk_wait_group0();  // the tile has left shared memory before the CTA exits
+        // the tile has been read out of shared memory before the CTA exits
+        // (the global writes complete on their own)
+        bulk_wait_group_read0();
       }
     }
   } else {

@@ -157,12 +157,19 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
                     qbase0 + i * kBM, bt);
       int n = 0, nk = 0;
       bool ok = true;
+      // packed sequences of the two query tiles (fixed) and of the last key
+      // tile (the next one's first guess)
+      const SegInfo sq0 = seg_info(P, q0), sq1 = seg_info(P, q1, sq0.last);
+      int khint = sq0.first;
       auto visit = [&](int kt) {
         const TileSpan ks = tile_span(P, kt * kBN);
-        const int c0 = (disjoint(ks, w0.band) && disjoint(ks, w0.sink)) ? kEmpty
-                                                                      : classify(P, q0, ks);
-        const int c1 = (disjoint(ks, w1.band) && disjoint(ks, w1.sink)) ? kEmpty
-                                                                      : classify(P, q1, ks);
+        const bool out0 = disjoint(ks, w0.band) && disjoint(ks, w0.sink);
+        const bool out1 = disjoint(ks, w1.band) && disjoint(ks, w1.sink);
+        if (out0 && out1) return;
+        const SegInfo sk = seg_info(P, ks, khint);
+        khint = sk.last;
+        const int c0 = out0 ? kEmpty : classify(P, q0, sq0, ks, sk);
+        const int c1 = out1 ? kEmpty : classify(P, q1, sq1, ks, sk);
         if (c0 == kEmpty && c1 == kEmpty) return;
         const int slot = n & 1, use = n >> 1;
         if (use >= 1 && !(ok = mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1,
@@ -228,14 +235,20 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       const uint32_t s_tm[2] = {tmem, tmem + 128};
       const uint32_t o_tm[2] = {tmem + 256, tmem + 256 + kD};
       int cnt[2] = {0, 0};
+      // operand descriptors, built once (every tile of a buffer is a whole
+      // tile further on) and stepped by constants
+      const uint64_t dq0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t dp0 = sdesc_sw128(sbase + L::kP, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sbase + L::kV, 16, 1024);
       bool ok = mbar_wait(bar(L::kQFull), 0, abort_flag, P.status);
       auto qk = [&](int i, int slot) {
-        const uint32_t qa = sbase + L::kQ + i * L::kTileBytes;
-        const uint32_t ka = sbase + L::kK + slot * L::kTileBytes;
+        const uint64_t qd = sdesc_add(dq0, i * L::kTileBytes);
+        const uint64_t kd = sdesc_add(dk0, slot * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kD / 32; ++kk)
-          mma_ss_f8(s_tm[i], sdesc_sw128(qa + 32 * kk, 16, 1024),
-                    sdesc_sw128(ka + 32 * kk, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+          mma_ss_f8(s_tm[i], sdesc_add(qd, 32 * kk), sdesc_add(kd, 32 * kk), kIdQK,
+                    kk > 0 ? 1u : 0u);
         mma_commit(bar(L::kSFull + i));
         ++cnt[i];
       };
@@ -245,12 +258,11 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
         if (!mbar_wait(bar(L::kVFull + slot), use & 1, abort_flag, P.status))
           return false;
         tc_fence_after();
-        const uint32_t pa = sbase + L::kP + i * L::kTileBytes;
-        const uint32_t va = sbase + L::kV + slot * L::kTileBytes;
+        const uint64_t pd = sdesc_add(dp0, i * L::kTileBytes);
+        const uint64_t vd = sdesc_add(dv0, slot * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kBN / 32; ++kk)
-          mma_ss_f8(o_tm[i], sdesc_sw128(pa + 32 * kk, 16, 1024),
-                    sdesc_sw128(va + 32 * kk, 16, 1024), kIdPV,
+          mma_ss_f8(o_tm[i], sdesc_add(pd, 32 * kk), sdesc_add(vd, 32 * kk), kIdPV,
                     (first && kk == 0) ? 0u : 1u);
         return true;
       };
@@ -459,7 +471,9 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
           for (int hf = 0; hf < 2; ++hf)
             tma_store_4d(&tm_o, smem_u32(stage[hf]), hf * 64, h, qbase0 + i * kBM, bt);
           bulk_commit_group();
-          bulk_wait_group0();
+          // the tile has been read out of shared memory before the CTA exits
+          // (the global writes complete on their own)
+          bulk_wait_group_read0();
         }
       }
       P.lse[lse_index(P, bt, h, prow)] =

@@ -299,6 +299,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The descriptor of the same tile `bytes` further on. The start address
+// (16-byte units) is the descriptor's low field, so while the address stays
+// inside the shared-memory window this is one add: descriptors are built
+// once per buffer and stepped with constants, which keeps the issuing
+// thread's work per MMA to a few instructions (rebuilding both descriptors
+// for every MMA made the issuing thread, not the tensor core, set the pace).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 // a_mn_major / b_mn_major select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major,

@@ -29,16 +29,38 @@ __device__ __forceinline__ TileSpan tile_span(const AttnParams& P, int base) {
   return t;
 }
 
-// empty / full / masked for query tile q against key tile k.
+// Packed sequences met by a tile: the indices of the sequences holding its
+// first and last positions, and the first one's start (all 0 when dense).
+struct SegInfo {
+  int first, last, start;
+};
+// `hint` is a sequence index to try first (the previous tile's, since tiles
+// are mostly visited in increasing position); the binary search runs only
+// when the hint misses.
+__device__ __forceinline__ SegInfo seg_info(const AttnParams& P, const TileSpan& t,
+                                            int hint = -1) {
+  SegInfo r{0, 0, 0};
+  if (P.cu == nullptr) return r;
+  if (hint >= 0 && hint < P.nseq && __ldg(P.cu + hint) <= t.lo && t.lo < __ldg(P.cu + hint + 1))
+    r.first = hint;
+  else
+    r.first = seg_of(P.cu, P.nseq, t.lo);
+  r.start = __ldg(P.cu + r.first);
+  r.last = t.hi < __ldg(P.cu + r.first + 1) ? r.first : seg_of(P.cu, P.nseq, t.hi);
+  return r;
+}
+
+// empty / full / masked for query tile q against key tile k, given the
+// sequences each meets (seg_info).
 __device__ __forceinline__ int classify(const AttnParams& P, const TileSpan& q,
-                                        const TileSpan& k) {
+                                        const SegInfo& qs, const TileSpan& k,
+                                        const SegInfo& ks) {
   int qlo = q.lo, qhi = q.hi, klo = k.lo, khi = k.hi;
   if (P.cu != nullptr) {
-    int sq0 = seg_of(P.cu, P.nseq, qlo), sq1 = seg_of(P.cu, P.nseq, qhi);
-    int sk0 = seg_of(P.cu, P.nseq, klo), sk1 = seg_of(P.cu, P.nseq, khi);
-    if (sk1 < sq0 || sk0 > sq1) return kClsEmpty;
-    if (!(sq0 == sq1 && sk0 == sk1 && sq0 == sk0)) return kClsMasked;
-    int st = __ldg(P.cu + sq0);
+    if (ks.last < qs.first || ks.first > qs.last) return kClsEmpty;
+    if (!(qs.first == qs.last && ks.first == ks.last && qs.first == ks.first))
+      return kClsMasked;
+    const int st = qs.start;
     qlo -= st; qhi -= st; klo -= st; khi -= st;
   }
   if (P.causal && klo > qhi) return kClsEmpty;
@@ -51,6 +73,12 @@ __device__ __forceinline__ int classify(const AttnParams& P, const TileSpan& q,
     full = full && all_window;
   }
   return full ? kClsFull : kClsMasked;
+}
+
+// The same, looking the sequences up.
+__device__ __forceinline__ int classify(const AttnParams& P, const TileSpan& q,
+                                        const TileSpan& k) {
+  return classify(P, q, seg_info(P, q), k, seg_info(P, k));
 }
 
 struct PosRange {
