@@ -544,7 +544,7 @@ usp_status_t usp_attn_decode(const void* q, const void* k, const void* v, void* 
   if (S % n_part != 0 || (S / n_part) % decode_keys_per_tile() != 0)
     return USP_ERR_INVALID_ARG;
   if (tree_order && n_part > 64) return USP_ERR_INVALID_ARG;
-  if (B > 65535 || Hkv > 65535) return USP_ERR_UNSUPPORTED;
+  if (B > 65535 || n_part > 65535) return USP_ERR_UNSUPPORTED;  // grid z and y
   if (B > 0 && (!q || !k || !v || !out || !lse)) return USP_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, lse, workspace};
   for (const void* p : ptrs)

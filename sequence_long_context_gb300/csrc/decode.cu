@@ -12,17 +12,22 @@
 // merge then combines the pieces in key order (tree order: pairwise levels,
 // so the pieces of one shard meet first, then the shards).
 //
-// HBM-bound: every cached key and value is read once. A CTA streams its piece
-// through shared memory in tiles of 64 keys (TMA, 128-byte swizzle, two
-// stages filled by a producer warp, three CTAs per SM). Each of the four
-// compute warps takes 16 keys of every tile and runs its own online softmax
-// over them, so no block-wide barrier is needed inside the loop:
-//   scores   a lane pair per key, each lane of the pair takes half of D;
-//            q rows are held in shared memory pre-scaled by scale * log2(e)
+// HBM-bound: every cached key and value is read once. A CTA (one per SM)
+// streams its piece through shared memory in tiles of 64 keys (TMA, 128-byte
+// swizzle, five stages filled by a producer warp). Tile i belongs to the
+// pair of compute warps i mod 5, each taking 32 of its keys; every warp runs its
+// own online softmax over its keys, so no block-wide barrier is needed
+// inside the loop:
+//   scores   a lane pair per key, each lane of the pair takes half of D and
+//            keys p and p + 16 of the warp's 32 (one at a time when there
+//            are more than eight query rows), so a chunk of q, held in
+//            shared memory pre-scaled by scale * log2(e), is read once for
+//            two keys
 //   softmax  running max m and sum l per query row by warp shuffles,
-//            P = 2^(s - m) to a warp-private buffer, O rescaled
+//            P = 2^(s - m) to a warp-private buffer (key-major: a key's row
+//            values are one vector read), O rescaled
 //   P V      lanes own output columns
-// At the end the four warps' (m, l, O) are merged with the log-sum-exp rule.
+// At the end the warps' (m, l, O) are merged with the log-sum-exp rule.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -37,11 +42,18 @@ using namespace tc;
 
 __device__ int g_decode_status = 0;
 
-constexpr int kComputeWarps = 4;
+constexpr int kKeys = 64;           // keys per tile
+constexpr int kMaxRows = 16;        // G * Tq
+constexpr int kStages = 5;          // K/V tiles in flight per CTA (one CTA per SM)
+constexpr int kWarpsPerTile = 2;    // a tile's keys are split between two warps
+constexpr int kWarpKeys = kKeys / kWarpsPerTile;
+constexpr int kComputeWarps = kStages * kWarpsPerTile;
 constexpr int kThreads = 32 * (kComputeWarps + 1);  // + one producer warp
-constexpr int kKeys = 64;     // keys per tile
-constexpr int kMaxRows = 16;  // G * Tq
-constexpr int kStages = 2;    // K/V tiles in flight per CTA (three CTAs fit an SM)
+
+// keys scored together by a lane pair (sharing each chunk of q): both of
+// its keys, or one when the rows' accumulators would not fit the registers
+template <int R>
+__host__ __device__ constexpr int keys_together() { return R <= 8 ? 2 : 1; }
 
 struct DecodeParams {
   const __nv_bfloat16* q;  // [B][Tq][Hq][D]
@@ -71,8 +83,8 @@ struct DSmem {
   static constexpr int kK = 0;                      // kStages stages
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kQ = kV + kStages * kTileBytes;  // [R] padded rows, fp32
-  static constexpr int kP = kQ + R * kQStride<D>() * 4;  // per warp [R][16] fp32
-  static constexpr int kMerge = kP + kComputeWarps * R * 16 * 4;  // per warp m, l [R]
+  static constexpr int kP = kQ + R * kQStride<D>() * 4;  // per warp [kWarpKeys][R] fp32
+  static constexpr int kMerge = kP + kComputeWarps * kWarpKeys * R * 4;  // per warp m, l [R]
   static constexpr int kBar = kMerge + 2 * kComputeWarps * kMaxRows * 4;
   static constexpr int kMisc = kBar + 8 * 2 * kStages;  // abort flag
   static constexpr int kBytes = kMisc + 16;
@@ -80,6 +92,7 @@ struct DSmem {
   static_assert(kBar % 8 == 0, "barriers need 8-byte alignment");
   static_assert(kComputeWarps * R * D * 4 <= 2 * kStages * kTileBytes,
                 "the final merge fits the tiles");
+  static_assert(kP % 16 == 0, "vector reads of P");
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
 };
 
@@ -114,14 +127,16 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int piece = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // KV heads innermost: the CTAs of one piece, which together read whole
+  // cache rows (all heads of each key), run side by side
+  const int g = blockIdx.x, piece = blockIdx.y, b = blockIdx.z;
   const int key0 = piece * P.piece;
   const int ntiles = P.piece / kKeys;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), kComputeWarps);  // one arrival per compute warp
+      mbar_init(empty(s), kWarpsPerTile);  // the warps that share the stage's tile
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -149,7 +164,7 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
-        // the stage is free once every compute warp has released tile i - kStages
+        // the stage is free once its warps have released tile i - kStages
         if (i >= kStages &&
             !mbar_wait(empty(st), (i / kStages - 1) & 1, abort_flag, P.status))
           break;
@@ -170,10 +185,15 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
     }
   } else {
     // ---------------------------------------------------------- compute warps
-    // Each warp runs its own online softmax over its 16 keys of every tile:
-    // running max m, running sum l and the O accumulator (packed fp32 pairs,
-    // lane owns columns kCols*lane ..), merged across warps at the end.
-    float* pw = reinterpret_cast<float*>(sm + L::kP) + warp * R * 16;  // [R][16]
+    // Each warp runs its own online softmax over its keys of its tiles
+    // (tiles i = warp / 2, warp / 2 + 5, ..., keys [32 h, 32 h + 32) with
+    // h = warp mod 2): running max m, running sum l and the O accumulator
+    // (packed fp32 pairs, lane owns columns kCols*lane ..), merged across
+    // warps at the end.
+    constexpr int KG = keys_together<R>();
+    constexpr int kPasses = kWarpKeys / 16;
+    const int kbase = (warp % kWarpsPerTile) * kWarpKeys;
+    float* pw = reinterpret_cast<float*>(sm + L::kP) + warp * kWarpKeys * R;  // [kWarpKeys][R]
     float m[R], l[R];
     uint64_t o2[R][kPairs];
 #pragma unroll
@@ -184,89 +204,131 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
       for (int j = 0; j < kPairs; ++j) o2[r][j] = 0ull;
     }
     const int qpos0 = P.S - P.Tq;  // position of token t = 0
-    const int kk = warp * 16 + (lane & 15), hs = lane >> 4;
+    const int pr = lane & 15, hs = lane >> 4;
     const int col = kCols * lane;
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = warp / kWarpsPerTile; i < ntiles; i += kStages) {
       const int st = i % kStages;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(full(st), (i / kStages) & 1, abort_flag, P.status);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       const uint8_t* kt = sm + L::kK + st * L::kTileBytes;
       const uint8_t* vt = sm + L::kV + st * L::kTileBytes;
-      const int kpos = key0 + i * kKeys + kk;
-      // scores: a lane pair per key, each lane half of D
-      uint64_t acc2[R];
+      // the warp's keys in passes of 16 KG: the lane pair's keys
+      // kbase + pr + 16 (jb + g), g < KG
 #pragma unroll
-      for (int r = 0; r < R; ++r) acc2[r] = 0ull;
+      for (int jb = 0; jb < kPasses; jb += KG) {
+        // scores: a lane pair per key, each lane half of D
+        uint64_t acc2[KG][R];
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        const int chunk = hs * (D / 16) + c;
-        const uint4 raw = *reinterpret_cast<const uint4*>(tile_row<D>(kt, kk, chunk));
-        const uint64_t k0 = bf2_to_f2(raw.x), k1 = bf2_to_f2(raw.y);
-        const uint64_t k2 = bf2_to_f2(raw.z), k3 = bf2_to_f2(raw.w);
+        for (int g = 0; g < KG; ++g)
+#pragma unroll
+          for (int r = 0; r < R; ++r) acc2[g][r] = 0ull;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          const int chunk = hs * (D / 16) + c;
+          uint64_t kr[KG][4];
+#pragma unroll
+          for (int g = 0; g < KG; ++g) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(
+                tile_row<D>(kt, kbase + pr + 16 * (jb + g), chunk));
+            kr[g][0] = bf2_to_f2(raw.x);
+            kr[g][1] = bf2_to_f2(raw.y);
+            kr[g][2] = bf2_to_f2(raw.z);
+            kr[g][3] = bf2_to_f2(raw.w);
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float* qp = qs + q_index<D>(r, chunk * 8);
+            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qp);
+            const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qp + 4);
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+              acc2[g][r] = f2_fma(qa.x, kr[g][0], acc2[g][r]);
+              acc2[g][r] = f2_fma(qa.y, kr[g][1], acc2[g][r]);
+              acc2[g][r] = f2_fma(qb.x, kr[g][2], acc2[g][r]);
+              acc2[g][r] = f2_fma(qb.y, kr[g][3], acc2[g][r]);
+            }
+          }
+        }
+        // softmax over the pass's 16 KG keys (both lane halves hold the same
+        // values after the first reduction; later ones stay within a half)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const float* qp = qs + q_index<D>(r, chunk * 8);
-          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qp);
-          const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qp + 4);
-          acc2[r] = f2_fma(qa.x, k0, acc2[r]);
-          acc2[r] = f2_fma(qa.y, k1, acc2[r]);
-          acc2[r] = f2_fma(qb.x, k2, acc2[r]);
-          acc2[r] = f2_fma(qb.y, k3, acc2[r]);
+          float sc[KG];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < KG; ++g) {
+            float lo, hi;
+            f2_unpack(acc2[g][r], lo, hi);
+            float x = lo + hi;
+            x += __shfl_xor_sync(0xffffffffu, x, 16);
+            const int kpos = key0 + i * kKeys + kbase + pr + 16 * (jb + g);
+            if (P.causal && kpos > qpos0 + r % P.Tq) x = -INFINITY;
+            sc[g] = x;
+            mx = fmaxf(mx, x);
+          }
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          const float m_new = fmaxf(m[r], mx);
+          float a = 1.f, sum = 0.f;
+          float pg[KG];
+#pragma unroll
+          for (int g = 0; g < KG; ++g) pg[g] = 0.f;
+          if (m_new != -INFINITY) {
+            a = (m[r] == -INFINITY) ? 0.f : ex2(m[r] - m_new);
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+              pg[g] = (sc[g] == -INFINITY) ? 0.f : ex2(sc[g] - m_new);
+              sum += pg[g];
+            }
+          }
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+          l[r] = l[r] * a + sum;
+          m[r] = m_new;
+          const uint64_t a2 = f2_pack(a, a);
+#pragma unroll
+          for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(o2[r][j], a2, 0ull);
+          if (hs == 0) {
+#pragma unroll
+            for (int g = 0; g < KG; ++g) pw[(pr + 16 * (jb + g)) * R + r] = pg[g];
+          }
         }
-      }
-      // softmax over the warp's 16 keys (both lane halves hold the same
-      // values after the first reduction; later ones stay within a half)
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float lo, hi;
-        f2_unpack(acc2[r], lo, hi);
-        float sc = lo + hi;
-        sc += __shfl_xor_sync(0xffffffffu, sc, 16);
-        if (P.causal && kpos > qpos0 + r % P.Tq) sc = -INFINITY;
-        float mx = sc;
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float m_new = fmaxf(m[r], mx);
-        float a = 1.f, p = 0.f;
-        if (m_new != -INFINITY) {
-          a = (m[r] == -INFINITY) ? 0.f : ex2(m[r] - m_new);
-          p = (sc == -INFINITY) ? 0.f : ex2(sc - m_new);
-        }
-        float sum = p;
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        l[r] = l[r] * a + sum;
-        m[r] = m_new;
-        const uint64_t a2 = f2_pack(a, a);
-#pragma unroll
-        for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(o2[r][j], a2, 0ull);
-        if (hs == 0) pw[r * 16 + (lane & 15)] = p;
-      }
-      __syncwarp();
-      // P V over the warp's 16 keys, lane owns columns
+        __syncwarp();
+        // P V over the pass's keys, lane owns columns
 #pragma unroll 4
-      for (int k16 = 0; k16 < 16; ++k16) {
-        const int key = warp * 16 + k16;
-        const uint8_t* src = tile_row<D>(vt, key, col >> 3) + (col & 7) * 2;
-        uint64_t v2[kPairs];
-        if constexpr (kPairs == 2) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(src);
-          v2[0] = bf2_to_f2(raw.x);
-          v2[1] = bf2_to_f2(raw.y);
-        } else {
-          v2[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(src));
-        }
+        for (int kk = 16 * jb; kk < 16 * (jb + KG); ++kk) {
+          const uint8_t* src = tile_row<D>(vt, kbase + kk, col >> 3) + (col & 7) * 2;
+          uint64_t v2[kPairs];
+          if constexpr (kPairs == 2) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(src);
+            v2[0] = bf2_to_f2(raw.x);
+            v2[1] = bf2_to_f2(raw.y);
+          } else {
+            v2[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(src));
+          }
+          float pv[R];
+          if constexpr (R % 4 == 0) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float pp = pw[r * 16 + k16];
-          const uint64_t p2 = f2_pack(pp, pp);
+            for (int r4 = 0; r4 < R / 4; ++r4) {
+              const float4 x = *reinterpret_cast<const float4*>(pw + kk * R + 4 * r4);
+              pv[4 * r4] = x.x; pv[4 * r4 + 1] = x.y; pv[4 * r4 + 2] = x.z; pv[4 * r4 + 3] = x.w;
+            }
+          } else {
 #pragma unroll
-          for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(p2, v2[j], o2[r][j]);
+            for (int r = 0; r < R; ++r) pv[r] = pw[kk * R + r];
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const uint64_t p2 = f2_pack(pv[r], pv[r]);
+#pragma unroll
+            for (int j = 0; j < kPairs; ++j) o2[r][j] = f2_fma(p2, v2[j], o2[r][j]);
+          }
         }
+        __syncwarp();  // the P buffer is reused by the next pass
       }
-      __syncwarp();  // this warp is done with the stage and with its P buffer
-      if (lane == 0) mbar_arrive(empty(st));
+      if (lane == 0) mbar_arrive(empty(st));  // this warp is done with the stage
     }
     // every compute warp is done with the tiles (named barrier of the four
     // compute warps, reached on the abort path too) before the partials
@@ -371,7 +433,7 @@ usp_status_t launch_d(const DecodeParams& P, const void* k, const void* v, cudaS
   }
   DecodeParams Pk = P;
   Pk.status = status;
-  dim3 grid(P.n_part, P.Hkv, P.B);
+  dim3 grid(P.Hkv, P.n_part, P.B);
   auto go = [&](auto kernel, int smem) -> usp_status_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smem);
