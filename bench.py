@@ -1,12 +1,14 @@
 """Benchmark of the sequence-parallel attention hot path on GB300.
 
 One step is one training pass of the whole path over one batch of synthetic
-input, through the library's C ABI:
-  extract q, k, v, dO into rank-major order (layout permute)
-  -> usp_attn_fwd  (Ulysses seq->head exchange, ring attention with the
-                    fused LSE merge, head->seq exchange)
-  -> usp_attn_bwd  (exchanges, Delta, dQ/dK/dV with the ring return)
-  -> restore O, dQ, dK, dV to natural order.
+input in natural sequence order, through the library's C ABI:
+  usp_attn_fwd  (extract q, k, v into rank-major order fused with the
+                 Ulysses seq->head exchange, ring attention with the fused
+                 LSE merge, head->seq exchange fused with the restore of O)
+  -> usp_attn_bwd  (the same for dO in and dQ, dK, dV out, reusing the
+                    forward's copies of q, k, v, O; Delta, dQ/dK/dV with the
+                    ring return).
+Without Ulysses (ud = 1) the extract and restore run as layout permutes.
 The metric is useful attention TFLOP/s (masked pairs not counted; backward
 = 2.5x forward). The standalone tree/linear LSE merge is timed on its own
 workload in the same run and reported under "merge".
@@ -271,26 +273,28 @@ def run_reference(args):
     print(json.dumps(line))
 
 
-def make_step(usp, w, x, cu_dev):
+def make_step(usp, w, x, cu_dev, keep=None):
     """One training pass of workload w over the natural-order inputs `inp`:
-    extract, forward, backward (reusing the forward's Ulysses exchange from
-    the shared workspace), restore. Returns the natural-order results."""
+    forward and backward on natural-order tensors (the layout's extract and
+    restore inside the calls, fused with the Ulysses exchange), the backward
+    reusing the forward's rank-major copies of q, k, v, out from the shared
+    workspace. Returns the natural-order results [O(, dQ, dK, dV)]; `keep`
+    (a dict), if given, receives each step's LSE under "lse"."""
     kw = dict(causal=w.causal, window=w.window, sink_tokens=w.sink_tokens,
-              cu_seqlens=cu_dev, cp=w.cp, ud=w.ud, layout=w.layout)
-    # one workspace for the forward and the backward of every step: the
-    # backward reads the forward's head-sharded q, k, v, out from it instead
-    # of exchanging them again
-    ws = usp.attn_workspace(x["q"], x["k"], cu_seqlens=cu_dev, cp=w.cp, ud=w.ud)
+              cu_seqlens=cu_dev, cp=w.cp, ud=w.ud, layout=w.layout, natural=True)
+    # one workspace for the forward and the backward of every step
+    ws = usp.attn_workspace(x["q"], x["k"], cu_seqlens=cu_dev, cp=w.cp, ud=w.ud,
+                            natural=True)
 
     def step(inp):
-        qp, kp, vp = (usp.permute(inp[n], "extract", w.layout, w.cp) for n in "qkv")
-        out, lse = usp.attn_forward(qp, kp, vp, workspace=ws, **kw)
+        out, lse = usp.attn_forward(inp["q"], inp["k"], inp["v"], workspace=ws, **kw)
+        if keep is not None:
+            keep["lse"] = lse
         res = [out]
         if w.backward:
-            dop = usp.permute(inp["dout"], "extract", w.layout, w.cp)
-            res += list(usp.attn_backward(qp, kp, vp, out, lse, dop, workspace=ws,
-                                          saved_exchange=True, **kw))
-        return [usp.permute(r, "restore", w.layout, w.cp) for r in res]
+            res += list(usp.attn_backward(inp["q"], inp["k"], inp["v"], out, lse, inp["dout"],
+                                          workspace=ws, saved_exchange=True, **kw))
+        return res
 
     return step
 
@@ -434,17 +438,13 @@ def main():
     elem = 2 if w.dtype == "bf16" else 4
     q_bytes = (1 if w.varlen else w.B) * w.S * w.Hq * w.D * elem
     kv_bytes = (1 if w.varlen else w.B) * w.S * w.Hkv * w.D * elem
-    # tensor bytes moved per step by each permute family (each byte is read
-    # once and written once): extract q,k,v(,dO), restore O(,dQ,dK,dV); the
-    # Ulysses exchange inside the attention calls when ud > 1: q, k, v in and
-    # out back in the forward; the backward reuses the forward's exchange
-    # (saved_exchange) and moves dO in and dQ, dK, dV back.
-    if w.backward:
-        moved = {"permute_layout": 4 * q_bytes + 4 * kv_bytes,
-                 "permute_ulysses": 4 * q_bytes + 4 * kv_bytes}
-    else:
-        moved = {"permute_layout": 2 * q_bytes + 2 * kv_bytes,
-                 "permute_ulysses": 2 * q_bytes + 2 * kv_bytes}
+    # tensor bytes moved per step (each byte is read once and written once):
+    # q, k, v in and O out in the forward; the backward reuses the forward's
+    # copies (saved_exchange) and moves dO in and dQ, dK, dV out. With
+    # Ulysses the layout's extract / restore ride along with the exchange
+    # (permute_ulysses); without, they are the layout permutes.
+    fam = "permute_ulysses" if w.ud > 1 else "permute_layout"
+    moved = {fam: (4 if w.backward else 2) * (q_bytes + kv_bytes)}
     for k, mv in moved.items():
         if k in kernels:
             per_launch = 2 * mv / kernels[k]["launches_per_step"]

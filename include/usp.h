@@ -106,6 +106,20 @@ typedef enum {
  * the workspace are trusted: a workspace that does not hold that forward's
  * exchange gives wrong gradients, not an error. */
 #define USP_FLAG_SAVED_EXCHANGE 2u
+/* usp_attn_fwd / usp_attn_bwd (and usp_attn_bwd_noalloc): q, k, v, out,
+ * dout, dq, dk and dv are in natural sequence order instead of rank-major
+ * order; lse stays rank-major (it is the forward's state for the backward).
+ * The result equals extracting the inputs (USP_PERMUTE_EXTRACT), calling
+ * without the flag and restoring the outputs (USP_PERMUTE_RESTORE), bit for
+ * bit. With ulysses_degree > 1 the extract and restore ride along with the
+ * Ulysses exchange, so each tensor is moved once instead of twice; with
+ * ulysses_degree == 1 the kernels work on rank-major copies in the
+ * workspace (usp_attn_*_workspace_size must be given the flag). Combined
+ * with USP_FLAG_SAVED_EXCHANGE the backward also reuses those copies of
+ * q, k, v, out at ulysses_degree == 1. Not supported by the q/k/v-packed
+ * entry points and usp_attn_fwd_fp8 (USP_ERR_UNSUPPORTED). Forward and
+ * backward must be given the same flags. */
+#define USP_FLAG_NATURAL_ORDER 4u
 
 /*
  * usp_attn_fwd - ring attention forward with the fused LSE merge.
@@ -122,8 +136,9 @@ typedef enum {
  * heads, and the output is exchanged head->sequence back into `out`.
  *
  * q    [B, S, Hq, D]   (packed: [S, Hq, D], S = total tokens T), rank-major
- * k, v [B, S, Hkv, D]  (packed: [S, Hkv, D]), rank-major, same layout as q
- * out  [B, S, Hq, D]   written, rank-major, dtype as q
+ *      (natural order with USP_FLAG_NATURAL_ORDER)
+ * k, v [B, S, Hkv, D]  (packed: [S, Hkv, D]), same order and layout as q
+ * out  [B, S, Hq, D]   written, in q's sequence order, dtype as q
  * lse  [B, Hq, S] fp32 written (packed: [Hq, S]), natural log of the scaled
  *      scores' sum of exponentials, rank-major sequence order
  * B, S, Hq, Hkv, D   D in {64, 128}; Hq % Hkv == 0 (query head h reads KV
@@ -147,7 +162,8 @@ typedef enum {
  *      ulysses_degree > 1 it holds the head-sharded q, k, v and out on
  *      return (what USP_FLAG_SAVED_EXCHANGE lets the backward reuse).
  * Errors: USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, USP_ERR_WORKSPACE,
- *      USP_ERR_UNSUPPORTED (fp32 with D not in {64,128}), USP_ERR_CUDA.
+ *      USP_ERR_UNSUPPORTED (D not in {64,128}; USP_FLAG_NATURAL_ORDER from
+ *      the packed entry point), USP_ERR_CUDA.
  */
 usp_status_t usp_attn_fwd(const void *q, const void *k, const void *v,
                           void *out, float *lse, int B, int S, int Hq, int Hkv,
@@ -176,7 +192,8 @@ size_t usp_attn_fwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
  * q, k, v, out, lse: as passed to / produced by usp_attn_fwd (same args);
  *      with USP_FLAG_SAVED_EXCHANGE and ulysses_degree > 1, q, k, v, out are
  *      read from the forward's workspace instead (see the flag).
- * dout [B,S,Hq,D] rank-major, dtype as q. dq/dk/dv written, shapes of q/k/v.
+ * dout [B,S,Hq,D] in q's sequence order, dtype as q. dq/dk/dv written,
+ *      shapes and order of q/k/v.
  * Scalar arguments must equal those of the forward call.
  * Errors: as usp_attn_fwd.
  */
@@ -316,7 +333,8 @@ usp_status_t usp_attn_bwd_qkvpacked(const void *qkv, const void *out,
  *      usp_attn_fwd (packed [T,H,128] with cu_seqlens), 16-byte aligned.
  * q_descale, k_descale, v_descale  finite, > 0 (else USP_ERR_INVALID_ARG).
  * out  [B,S,Hq,128] bf16, written.  lse  as in usp_attn_fwd.
- * Other arguments as in usp_attn_fwd (dtype is implied; flags unused).
+ * Other arguments as in usp_attn_fwd (dtype is implied; flags: none
+ *      apply, USP_FLAG_NATURAL_ORDER gives USP_ERR_UNSUPPORTED).
  * workspace  at least usp_attn_fwd_fp8_workspace_size(...) bytes, 16-byte
  *      aligned, never NULL for S > 0 (it holds V transposed to
  *      [B][Hkv][128][S]); contents on entry irrelevant.

@@ -22,6 +22,7 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 PERMUTE = {"extract": 0, "restore": 1, "seq2head": 2, "head2seq": 3}
 FLAG_FORCE_SIMT = 1
 FLAG_SAVED_EXCHANGE = 2
+FLAG_NATURAL_ORDER = 4
 
 
 class UspError(RuntimeError):
@@ -275,10 +276,14 @@ def _use_workspace(workspace, need, device):
     return workspace, workspace.numel()
 
 
-def attn_workspace(q, k, *, cu_seqlens=None, cp=1, ud=1, flags=0) -> torch.Tensor:
+def attn_workspace(q, k, *, cu_seqlens=None, cp=1, ud=1, flags=0,
+                   natural=False) -> torch.Tensor:
     """A workspace that fits both attn_forward and attn_backward of these
     shapes. Passing the same one to both, and saved_exchange=True to the
-    backward, lets the backward reuse the forward's Ulysses exchange."""
+    backward, lets the backward reuse the forward's Ulysses exchange (or,
+    natural=True, its rank-major copies)."""
+    if natural:
+        flags |= FLAG_NATURAL_ORDER
     B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
     n = usp_attn_bwd_workspace_size(Bl, S, Hq, Hkv, D, cp, ud, q.dtype, flags)
     return torch.empty(n, dtype=torch.uint8, device=q.device)
@@ -286,9 +291,14 @@ def attn_workspace(q, k, *, cu_seqlens=None, cp=1, ud=1, flags=0) -> torch.Tenso
 
 def attn_forward(q, k, v, *, causal=True, window=0, sink_tokens=0,
                  cu_seqlens=None, cp=1, ud=1, layout="contiguous",
-                 softmax_scale=0.0, flags=0, workspace=None, stream=None
-                 ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """(out, lse) for rank-major q/k/v ([B,S,H,D] or packed [T,H,D])."""
+                 softmax_scale=0.0, flags=0, workspace=None, stream=None,
+                 natural=False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(out, lse) for rank-major q/k/v ([B,S,H,D] or packed [T,H,D]);
+    natural=True: q/k/v and out in natural sequence order (lse rank-major),
+    the layout's extract and restore done inside the call
+    (FLAG_NATURAL_ORDER)."""
+    if natural:
+        flags |= FLAG_NATURAL_ORDER
     B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
     out = torch.empty_like(q)
     lse = torch.empty((Bl, Hq, S) if cu_seqlens is None else (Hq, S),
@@ -305,10 +315,13 @@ def attn_forward(q, k, v, *, causal=True, window=0, sink_tokens=0,
 def attn_backward(q, k, v, out, lse, dout, *, causal=True, window=0,
                   sink_tokens=0, cu_seqlens=None, cp=1, ud=1,
                   layout="contiguous", softmax_scale=0.0, flags=0,
-                  workspace=None, saved_exchange=False, stream=None):
+                  workspace=None, saved_exchange=False, stream=None, natural=False):
     """(dq, dk, dv) for rank-major tensors and the forward's (out, lse).
     saved_exchange: workspace is the one the forward wrote (attn_workspace),
-    holding its head-sharded q, k, v, out (FLAG_SAVED_EXCHANGE)."""
+    holding its head-sharded q, k, v, out (FLAG_SAVED_EXCHANGE).
+    natural: as in attn_forward (every tensor but lse in natural order)."""
+    if natural:
+        flags |= FLAG_NATURAL_ORDER
     B, S, Hq, Hkv, D, Bl = _dims(q, k, cu_seqlens)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if saved_exchange:

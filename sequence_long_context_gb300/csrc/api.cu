@@ -101,6 +101,12 @@ bool aligned16(const void* p) {
 
 struct Shape {
   int B, S, Hq, Hkv, D, cp, ud, layout, dtype, varlen;
+  // USP_FLAG_NATURAL_ORDER: the caller's q, k, v, out, dout, dq, dk, dv are
+  // in natural sequence order (the kernels' copies in the workspace are
+  // rank-major)
+  int natural = 0;
+  // the kernels need workspace copies of the caller's tensors
+  bool staged() const { return ud > 1 || natural; }
   size_t elem() const { return dtype == USP_FP32 ? 4 : 2; }
   size_t q_bytes() const { return (size_t)B_eff() * S * Hq * D * elem(); }
   size_t kv_bytes() const { return (size_t)B_eff() * S * Hkv * D * elem(); }
@@ -175,7 +181,7 @@ struct FwdWs {
 };
 FwdWs carve_fwd(Carve& c, const Shape& s) {
   FwdWs w{};
-  if (s.ud > 1) {
+  if (s.staged()) {
     w.q = c.take(s.q_bytes());
     w.k = c.take(s.kv_bytes());
     w.v = c.take(s.kv_bytes());
@@ -195,7 +201,7 @@ struct BwdWs {
 // holds them where the backward reads them.
 BwdWs carve_bwd(Carve& c, const Shape& s, bool tc) {
   BwdWs w{};
-  if (s.ud > 1) {
+  if (s.staged()) {
     w.q = c.take(s.q_bytes());
     w.k = c.take(s.kv_bytes());
     w.v = c.take(s.kv_bytes());
@@ -206,7 +212,7 @@ BwdWs carve_bwd(Carve& c, const Shape& s, bool tc) {
     w.lse2 = static_cast<float*>(c.take((size_t)s.B_eff() * s.Hq * s.S * 4));
     w.dq_acc = static_cast<float*>(c.take((size_t)s.B_eff() * s.S * s.Hq * s.D * 4));
   }
-  if (s.ud > 1) {
+  if (s.staged()) {
     w.dout = c.take(s.q_bytes());
     w.dq = c.take(s.q_bytes());
     w.dk = c.take(s.kv_bytes());
@@ -236,7 +242,19 @@ bool use_tc_bwd(const AttnParams& P, const Shape& s, unsigned flags) {
 usp_status_t a2a(const void* src, void* dst, const Shape& s, int H, int s2h,
                  cudaStream_t st, long long tok = 0) {
   return launch_ulysses(src, dst, s.B_eff(), s.S, (int)(H * s.D * s.elem()),
-                        s.ud, s2h, st, (int)(tok * s.elem()), 0);
+                        s.ud, s2h, st, (int)(tok * s.elem()), 0,
+                        s.natural ? s.layout : -1, s.cp);
+}
+
+// Into the kernels' rank-major copy (to_kernel) or back out of it, for one
+// [B,S,H,D] tensor of the caller: the Ulysses exchange when ud > 1 (with the
+// layout's extract / restore fused in for natural-order tensors), else the
+// layout's extract / restore alone.
+usp_status_t stage(const void* src, void* dst, const Shape& s, int H, int to_kernel,
+                   cudaStream_t st) {
+  if (s.ud > 1) return a2a(src, dst, s, H, to_kernel, st);
+  return launch_permute_layout(src, dst, s.B_eff(), s.S, (int)(H * s.D * s.elem()), s.layout,
+                               s.cp, to_kernel ? 0 : 1, st);
 }
 
 }  // namespace
@@ -318,8 +336,8 @@ int usp_profile_read(usp_kernel_stat_t* stats, int max_stats) {
 size_t usp_attn_fwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
                                    int cp, int ud, usp_dtype_t dtype,
                                    unsigned flags) {
-  (void)flags;
   Shape s = shape_of(B, S, Hq, Hkv, D, cp, ud, 0, dtype, 0);
+  s.natural = (flags & USP_FLAG_NATURAL_ORDER) != 0;
   Carve c(nullptr);
   carve_fwd(c, s);
   return c.used;
@@ -329,6 +347,7 @@ size_t usp_attn_bwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
                                    int cp, int ud, usp_dtype_t dtype,
                                    unsigned flags) {
   Shape s = shape_of(B, S, Hq, Hkv, D, cp, ud, 0, dtype, 0);
+  s.natural = (flags & USP_FLAG_NATURAL_ORDER) != 0;
   Carve c(nullptr);
   bool tc = dtype == USP_BF16 && !(flags & USP_FLAG_FORCE_SIMT);
   carve_bwd(c, s, tc);
@@ -347,8 +366,10 @@ usp_status_t attn_fwd_impl(const void* q, const void* k, const void* v,
                            size_t workspace_bytes, usp_stream_t stream, long long tok) {
   Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, dtype,
                      cu_seqlens != nullptr);
+  s.natural = (flags & USP_FLAG_NATURAL_ORDER) != 0;
   usp_status_t r = validate(s, window, sink_tokens);
   if (r != USP_OK) return r;
+  if (s.natural && tok != 0) return USP_ERR_UNSUPPORTED;  // packed q/k/v
   if (S > 0 && (!q || !k || !v || !out || !lse)) return USP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(lse) || !aligned16(workspace))
@@ -361,11 +382,16 @@ usp_status_t attn_fwd_impl(const void* q, const void* k, const void* v,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   AttnParams P = make_params(s, softmax_scale, causal, window, sink_tokens,
                              cu_seqlens);
-  if (s.ud > 1) {
+  if (s.ud > 1 && !s.natural) {
     if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
     if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
     if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
     P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o;  // dense head groups
+  } else if (s.staged()) {
+    if ((r = stage(q, w.q, s, Hq, 1, st)) != USP_OK) return r;
+    if ((r = stage(k, w.k, s, Hkv, 1, st)) != USP_OK) return r;
+    if ((r = stage(v, w.v, s, Hkv, 1, st)) != USP_OK) return r;
+    P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o;
   } else {
     P.q = q; P.k = k; P.v = v; P.o = out;
     P.qkv_tok = tok;
@@ -376,7 +402,7 @@ usp_status_t attn_fwd_impl(const void* q, const void* k, const void* v,
   else
     r = launch_fwd_simt(P, dtype == USP_BF16, st);
   if (r != USP_OK) return r;
-  if (s.ud > 1) r = a2a(w.o, out, s, Hq, 0, st);
+  if (s.staged()) r = stage(w.o, out, s, Hq, 0, st);
   return r;
 }
 
@@ -423,10 +449,13 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
                           size_t workspace_bytes, usp_stream_t stream, long long tok) {
   Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, dtype,
                      cu_seqlens != nullptr);
+  s.natural = (flags & USP_FLAG_NATURAL_ORDER) != 0;
   usp_status_t r = validate(s, window, sink_tokens);
   if (r != USP_OK) return r;
-  // saved: the workspace holds the forward's head-sharded q, k, v, out
-  const bool saved = (flags & USP_FLAG_SAVED_EXCHANGE) && s.ud > 1;
+  if (s.natural && tok != 0) return USP_ERR_UNSUPPORTED;  // packed q/k/v
+  // saved: the workspace holds the forward's copies of q, k, v, out (head
+  // groups, or rank-major copies of natural-order tensors)
+  const bool saved = (flags & USP_FLAG_SAVED_EXCHANGE) && s.staged();
   if (S > 0 && (!lse || !dout || !dq || !dk || !dv || (!saved && (!q || !k || !v || !out))))
     return USP_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv, workspace};
@@ -440,14 +469,20 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
   Carve c(workspace);
   BwdWs w = carve_bwd(c, s, tc);
   if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
-  if (s.ud > 1) {
+  if (s.staged()) {
     if (!saved) {
-      if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
-      if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
-      if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
-      if ((r = a2a(out, w.o, s, Hq, 1, st)) != USP_OK) return r;
+      if (s.natural) {
+        if ((r = stage(q, w.q, s, Hq, 1, st)) != USP_OK) return r;
+        if ((r = stage(k, w.k, s, Hkv, 1, st)) != USP_OK) return r;
+        if ((r = stage(v, w.v, s, Hkv, 1, st)) != USP_OK) return r;
+      } else {
+        if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
+        if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
+        if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
+      }
+      if ((r = stage(out, w.o, s, Hq, 1, st)) != USP_OK) return r;
     }
-    if ((r = a2a(dout, w.dout, s, Hq, 1, st)) != USP_OK) return r;
+    if ((r = stage(dout, w.dout, s, Hq, 1, st)) != USP_OK) return r;
     P.q = w.q; P.k = w.k; P.v = w.v; P.o = w.o; P.dout = w.dout;
     P.dq = w.dq; P.dk = w.dk; P.dv = w.dv;
   } else {
@@ -466,10 +501,14 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
   else
     r = launch_bwd_simt(P, dtype == USP_BF16, st);
   if (r != USP_OK) return r;
-  if (s.ud > 1) {
+  if (s.ud > 1 && !s.natural) {
     if ((r = a2a(w.dq, dq, s, Hq, 0, st, tok)) != USP_OK) return r;
     if ((r = a2a(w.dk, dk, s, Hkv, 0, st, tok)) != USP_OK) return r;
     if ((r = a2a(w.dv, dv, s, Hkv, 0, st, tok)) != USP_OK) return r;
+  } else if (s.staged()) {
+    if ((r = stage(w.dq, dq, s, Hq, 0, st)) != USP_OK) return r;
+    if ((r = stage(w.dk, dk, s, Hkv, 0, st)) != USP_OK) return r;
+    if ((r = stage(w.dv, dv, s, Hkv, 0, st)) != USP_OK) return r;
   }
   return USP_OK;
 }
@@ -600,11 +639,11 @@ usp_status_t usp_attn_fwd_fp8(const void* q, const void* k, const void* v, float
                               int cp_size, int ulysses_degree, usp_layout_t layout,
                               unsigned flags, void* workspace, size_t workspace_bytes,
                               usp_stream_t stream) {
-  (void)flags;
   Shape s = shape_of(B, S, Hq, Hkv, D, cp_size, ulysses_degree, layout, USP_BF16,
                      cu_seqlens != nullptr);
   usp_status_t r = validate(s, window, sink_tokens);
   if (r != USP_OK) return r;
+  if (flags & USP_FLAG_NATURAL_ORDER) return USP_ERR_UNSUPPORTED;
   if (!(q_descale > 0.f) || !(k_descale > 0.f) || !(v_descale > 0.f) ||
       !std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
     return USP_ERR_INVALID_ARG;

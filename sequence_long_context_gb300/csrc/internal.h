@@ -40,10 +40,14 @@ usp_status_t launch_permute_layout(const void* src, void* dst, int B, int S,
 // flat_row_bytes / flat_off_bytes: the [B*S] token rows of the flat side
 // (the source of seq2head, the destination of head2seq) are flat_row_bytes
 // apart and start flat_off_bytes in (0, 0: dense rows of row_bytes).
+// natural_layout >= 0: the flat side is in natural sequence order, the
+// grouped side rank-major for that layout over cp ring ranks (the layout's
+// extract / restore fused into the exchange); -1: both rank-major.
 usp_status_t launch_ulysses(const void* src, void* dst, int B, int S,
                             int row_bytes, int ud, int seq2head,
                             cudaStream_t st, int flat_row_bytes = 0,
-                            int flat_off_bytes = 0);
+                            int flat_off_bytes = 0, int natural_layout = -1,
+                            int cp = 1);
 
 // merge.cu
 usp_status_t launch_merge(const float* o_parts, const float* lse_parts, int n,

@@ -69,11 +69,15 @@ permute_layout_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
 }
 
 // Ulysses exchange: src [B*S][ud][rvu] <-> dst [ud][B*S][rvu] (16-byte
-// vectors); one warp per (group, token row).
+// vectors); one warp per (group, token row). With layout >= 0 the flat side
+// is in natural sequence order and the grouped side in rank-major order:
+// the layout's extract (seq2head) or restore (head2seq) rides along with the
+// exchange, so the tensor is moved once instead of twice.
 __global__ void __launch_bounds__(kThreads)
 ulysses_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                unsigned BS, unsigned rvu, unsigned ud, int seq2head,
-               unsigned flat_stride, unsigned flat_off) {
+               unsigned flat_stride, unsigned flat_off, unsigned S, int layout,
+               int cp, int shard, int chunk) {
   const unsigned lane = threadIdx.x & 31;
   const unsigned nwarps = gridDim.x * (kThreads / 32);
   const unsigned units = BS * ud;
@@ -81,9 +85,16 @@ ulysses_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
        t += nwarps) {
     const unsigned grp = t / BS, r = t - grp * BS;
     const size_t grouped = (size_t)(grp * BS + r) * rvu;  // [ud][B*S] order
+    // token row of the flat side: the same row, or (natural order) the row
+    // of the rank-major row's natural position
+    unsigned fr = r;
+    if (layout >= 0) {
+      const unsigned b = r / S, p = r - b * S;
+      fr = b * S + (unsigned)nat_pos((int)p, layout, cp, shard, chunk);
+    }
     // [B*S][ud] order; a token's row may sit inside a wider one (flat_stride
     // vectors per token, starting flat_off vectors in: a packed q/k/v tensor)
-    const size_t flat = (size_t)r * flat_stride + flat_off + (size_t)grp * rvu;
+    const size_t flat = (size_t)fr * flat_stride + flat_off + (size_t)grp * rvu;
     if (seq2head)
       warp_copy(src + flat, dst + grouped, rvu, lane);
     else
@@ -113,7 +124,8 @@ usp_status_t launch_permute_layout(const void* src, void* dst, int B, int S,
 
 usp_status_t launch_ulysses(const void* src, void* dst, int B, int S,
                             int row_bytes, int ud, int seq2head,
-                            cudaStream_t st, int flat_row_bytes, int flat_off_bytes) {
+                            cudaStream_t st, int flat_row_bytes, int flat_off_bytes,
+                            int natural_layout, int cp) {
   unsigned rvu = (unsigned)(row_bytes / ud / 16);
   if (flat_row_bytes == 0) flat_row_bytes = row_bytes;
   unsigned BS = (unsigned)B * (unsigned)S;
@@ -123,7 +135,8 @@ usp_status_t launch_ulysses(const void* src, void* dst, int B, int S,
     ulysses_kernel<<<grid_for((long long)BS * ud), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
         BS, rvu, (unsigned)ud, seq2head, (unsigned)(flat_row_bytes / 16),
-        (unsigned)(flat_off_bytes / 16));
+        (unsigned)(flat_off_bytes / 16), (unsigned)S, natural_layout, cp, S / cp,
+        natural_layout == kZigzag ? S / (2 * cp) : S / cp);
   }
   note_launch();
   return check_launch();

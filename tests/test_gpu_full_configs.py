@@ -1,5 +1,6 @@
 """GPU parity at the full problem sizes, in the benchmark's launch
-configuration (default flags: tensor-core kernels where they apply).
+configuration: the benchmark's own training step (natural-order forward and
+backward sharing one workspace, tensor-core kernels where they apply).
 
 The oracle cannot redo a full problem in seconds, so outputs are checked on
 seeded samples it computes one by one from the definition: O and LSE rows of
@@ -13,10 +14,11 @@ import numpy as np
 import pytest
 import torch
 
+import bench
 import sequence_long_context_gb300 as usp
 from oracle import attention
 from sequence_long_context_gb300.workloads import WORKLOADS, make_inputs
-from tests._gpu import TOL, device, lse_to_natural, rel_fro, run_backward, run_forward
+from tests._gpu import TOL, device, lse_to_natural, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -40,14 +42,17 @@ def test_full_config(name):
     dev = device()
     rng = np.random.default_rng(zlib.crc32(name.encode()))
     x = make_inputs(w, seed=0, device="cuda")
-    fwd = run_forward(usp, w, x, dev)
-    grads = run_backward(usp, w, x, dev, fwd) if w.backward else None
+    cu_dev = x.get("cu_seqlens")
+    kept = {}
+    res = bench.make_step(usp, w, x, cu_dev.to(dev) if cu_dev is not None else None,
+                          keep=kept)(x)
+    o_nat = res[0]
+    grads = tuple(res[1:]) if w.backward else None
     torch.cuda.synchronize()
     xc = {k: v.cpu() for k, v in x.items()}
     cu = xc.get("cu_seqlens")
     tol = TOL[w.dtype]
-    lse_nat = lse_to_natural(fwd[1].cpu().numpy().astype(np.float64), w)
-    o_nat = fwd[0]
+    lse_nat = lse_to_natural(kept["lse"].cpu().numpy().astype(np.float64), w)
     rows = sample_positions(w, rng)
     G = w.Hq // w.Hkv
     g = int(rng.integers(w.Hkv))

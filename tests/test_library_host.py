@@ -258,3 +258,29 @@ def test_noalloc_checks_arguments_first(lib, over, code):
                                   a["B"], a["S"], a["Hq"], 2, a["D"], 0.0, 1, 0, 0, None,
                                   a["cp"], 1, 1, 0, 0, None)
     assert st == code, lib.usp_status_string(st)
+
+
+def test_natural_order_flag_host_checks(lib):
+    N = usp.FLAG_NATURAL_ORDER
+    # ud = 1: the kernels' rank-major copies of q, k, v, out need scratch
+    assert usp.usp_attn_fwd_workspace_size(2, 8192, 32, 8, 128, 4, 1, 0) == 0
+    assert usp.usp_attn_fwd_workspace_size(2, 8192, 32, 8, 128, 4, 1, 0, N) == \
+        2 * 2 * 8192 * (32 + 8) * 128 * 2
+    # ud > 1: the exchange buffers serve as those copies, no extra scratch
+    for fn in (usp.usp_attn_fwd_workspace_size, usp.usp_attn_bwd_workspace_size):
+        assert fn(2, 8192, 32, 8, 128, 4, 2, 0, N) == fn(2, 8192, 32, 8, 128, 4, 2, 0)
+    # the backward's scratch still starts with the forward's (saved copies)
+    assert usp.usp_attn_bwd_workspace_size(1, 4096, 8, 2, 64, 2, 1, 1, N) >= \
+        usp.usp_attn_fwd_workspace_size(1, 4096, 8, 2, 64, 2, 1, 1, N)
+    # ud = 1 with the flag: the call gets as far as the missing workspace
+    assert fwd(lib, flags=N) == 4
+    assert bwd(lib, ud=1, flags=N) == 4
+    # saved copies at ud = 1: q, k, v, out may be NULL
+    assert bwd(lib, ud=1, flags=N | usp.FLAG_SAVED_EXCHANGE, q=None, k=None, v=None,
+               out=None) == 4
+    # the packed entry points and the e4m3 forward do not take it
+    assert lib.usp_attn_fwd_qkvpacked(FAKE, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0, 0, None, 4,
+                                      1, 1, 1, N, None, 0, None) == 2
+    assert lib.usp_attn_bwd_qkvpacked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0,
+                                      0, None, 4, 1, 1, 1, N, None, 0, None) == 2
+    assert fp8_fwd(lib, flags=N) == 2
