@@ -12,28 +12,29 @@
 // written once (the shard's ring return). dQ contributions are added into an
 // fp32 accumulator in global memory by TMA reduce-add operations.
 //
-// Roles (448 threads):
-//   warps 0-7  softmax groups, two threads per key row (each owns 64 of the
-//              128 query columns): P^T = exp2(S^T - LSE),
+// Roles (704 threads):
+//   warps 0-15  softmax, four threads per key row (warp w owns query columns
+//              [32 (w/4), 32 (w/4) + 32)): P^T = exp2(S^T - LSE),
 //              dS^T = P^T (dP^T - Delta); P^T and dS^T go back to tensor
 //              memory as bf16 (A operands of dV and dK) and dS to shared
-//              memory (A operand of dQ)
-//   warps 8-11 dQ group, one query row per thread: takes the dQ tile out of
+//              memory (A operand of dQ). No row reductions are needed (P
+//              comes from the saved LSE), so the columns split freely; four
+//              warps per TMEM lane quarter hide the latency of each phase
+//   warps 16-19 dQ group, one query row per thread: takes the dQ tile out of
 //              tensor memory (freeing it for the next tile's dP^T), stages
 //              it in the dS tile and the dO half of the tile's ring slot
 //              (both dead once the tile's dQ MMA is done), and has the TMA
 //              unit add it into the global fp32 accumulator; the dS tile
 //              and the dO half go back once the TMA has read them
-//   warp 12    producer: K, V once; then Q, dO tiles through a 2-slot ring.
+//   warp 20    producer: K, V once; then Q, dO tiles through a 2-slot ring.
 //              The Q half of a slot (Q tile, LSE and Delta rows) is refilled
 //              as soon as the tile's last MMA (dK, which reads Q) is done;
 //              the dO half once the dQ drain hands it back
-//   warp 13    MMA issuer and tensor-memory owner
-// Tensor memory (512 columns): S^T [0,128); queries 64g..64g+63 (softmax
-// group g) live in columns [64g, 64g+64) and are overwritten in place by
-// their P^T (bf16 pairs, first 32 columns) and dS^T (last 32); dP^T
-// [128,256), overwritten by dQ (fp32, D columns); dV [256, 256+D);
-// dK [256+D, 256+2D).
+//   warp 21    MMA issuer and tensor-memory owner
+// Tensor memory (512 columns): S^T [0,128); the 32 queries of column chunk
+// c live in columns [32c, 32c+32) and are overwritten in place by their P^T
+// (bf16 pairs, first 16 columns) and dS^T (last 16); dP^T [128,256),
+// overwritten by dQ (fp32, D columns); dV [256, 256+D); dK [256+D, 256+2D).
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -49,10 +50,11 @@ using namespace tc;
 
 __device__ int g_bwd_tc_status = 0;
 
-constexpr int kThreads = 448;
-constexpr int kDrainWarp0 = 8;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int kSoftWarps = 16;  // four per TMEM lane quarter, one per 32 queries
+constexpr int kDrainWarp0 = kSoftWarps;
+constexpr int kProducerWarp = kDrainWarp0 + 4;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = 32 * (kMmaWarp + 1);  // 704
 constexpr int kEnd = -1;
 
 template <int D>
@@ -116,9 +118,10 @@ __device__ __forceinline__ ColMask col_mask(const AttnParams& P, int j) {
   return m;
 }
 
-// 14 warps: four share a 16K-register sub-partition, so <= 128 each.
+// 22 warps: six share a 16K-register sub-partition, so <= 85 each (80 in
+// the allocation's steps of 8).
 template <int D>
-__global__ void __maxnreg__(128)
+__global__ void __maxnreg__(80)
 attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
@@ -157,7 +160,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     }
     mbar_init(bar(L::kSFull), 1);
     mbar_init(bar(L::kDPFull), 1);
-    mbar_init(bar(L::kDSFull), 2 * kTile / 32);  // one arrival per softmax warp
+    mbar_init(bar(L::kDSFull), kSoftWarps);  // one arrival per softmax warp
     mbar_init(bar(L::kDQFull), 1);
     mbar_init(bar(L::kDQEmpty), kTile / 32);  // one arrival per drain warp
     mbar_init(bar(L::kDQGroup), kTile);
@@ -170,7 +173,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
-    mbar_init(bar(L::kPReady), 2 * kTile / 32);  // one arrival per softmax warp
+    mbar_init(bar(L::kPReady), kSoftWarps);  // one arrival per softmax warp
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kKVStaged + s), kTile / 32);
     *abort_flag = 0;
     fence_barrier_init();
@@ -332,12 +335,13 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         }
         mma_commit(bar(L::kDPFull));
         // dV += P^T dO as soon as P^T is in tensor memory: it runs while the
-        // softmax warps compute dS (K dim = queries; A from tensor memory)
+        // softmax warps compute dS (K dim = queries; A from tensor memory:
+        // queries 32c .. 32c+31 as bf16 pairs in columns 32c .. 32c+15)
         if (!(ok = mbar_wait(bar(L::kPReady), n & 1, abort_flag, P.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dv, t_s + 8 * kk + 32 * (kk >> 2), sdesc_add(ddo_mn, slot_off + kk * 2048),
+          mma_ts(t_dv, t_s + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_add(ddo_mn, slot_off + kk * 2048),
                  kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
         if (!(ok = mbar_wait(bar(L::kDSFull), n & 1, abort_flag, P.status))) break;
         tc_fence_after();
@@ -347,11 +351,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           mma_ss(t_dp, sdesc_add(dds_mn, kk * 2048), sdesc_add(dk_mn, kk * 2048), kIdDQ,
                  kk > 0 ? 1u : 0u);
         mma_commit(bar(L::kDQFull));
-        // dK += dS^T Q
+        // dK += dS^T Q (dS^T of queries 32c .. 32c+31 in columns 32c+16 ..)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(t_dk, t_s + 32 + 8 * kk + 32 * (kk >> 2), sdesc_add(dq_mn, slot_off + kk * 2048),
-                 kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(t_dk, t_s + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                 sdesc_add(dq_mn, slot_off + kk * 2048), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kQEmpty + slot));
         ++n;
       }
@@ -366,17 +370,22 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       mma_commit(bar(L::kMmaDone));
       mbar_wait_drain(bar(L::kMmaDone), 0);
     }
-  } else if (warp < 8) {
+  } else if (warp < kSoftWarps) {
     // ------------------------------------------------------------ softmax
-    // Two groups share each key row: group `half` owns query columns
-    // [64 half, 64 half + 64) of S^T, dP^T, P^T, dS^T and of the dS tile.
-    const int half = warp >> 2, quarter = warp & 3;
+    // Four warps share each key row: warp w owns query columns
+    // [32 ch, 32 ch + 32), ch = w / 4, of S^T, dP^T and the dS tile, and
+    // columns [32 ch, 32 ch + 16) (P^T) and [32 ch + 16, 32 ch + 32) (dS^T)
+    // of the bf16 results over its dead S^T columns.
+    const int ch = warp >> 2, quarter = warp & 3;
+    const int half = ch;                // epilogue group (warps 0-7)
     const int j = quarter * 32 + lane;  // key row = TMEM lane
     const int kp = kt * kTile + j;      // permuted key row
     const ColMask cm = col_mask(P, nat_pos(P, kp));
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
-    uint8_t* ds_row = sm + L::kDS + j * 128;
+    const uint32_t t_s = tmem + lane_off + 32 * ch, t_dp = tmem + lane_off + 128 + 32 * ch;
+    // this warp's 16-byte chunks of row j of the 128B-swizzled MN-major dS
+    // tile: queries 32ch .. 32ch+31 are 8-query chunks 4ch .. 4ch+3
+    uint8_t* ds_row = sm + L::kDS + (ch >> 1) * L::kHalfBytes + j * 128;
     const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
     int c = 0;
     bool ok = true;
@@ -387,47 +396,40 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (e.x == kEnd) break;
       const int qt = e.x;
       const bool masked = e.z == kClsMasked;
+      // natural position of this warp's first query and the step between
       const TileSpan qs = tile_span(P, qt * kTile);
+      const int i_first = qs.lo + 32 * ch * qs.step;
       // this query tile's LSE (log2 units) and Delta, copied into the tile's
       // Q/dO slot by the producer with the tile itself
-      const float* lse2 = reinterpret_cast<const float*>(sm + L::kStats + (c & 1) * L::kStatBytes);
+      const float* lse2 = reinterpret_cast<const float*>(sm + L::kStats + (c & 1) * L::kStatBytes) + 32 * ch;
       const float* delta = lse2 + kTile;
       ok = mbar_wait(bar(L::kQFull + (c & 1)), (c >> 1) & 1, abort_flag, P.status);
       if (ok) ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // P^T (queries along columns) -> bf16 pairs. Each group writes only
-      // into its own 64 S^T columns (P^T over the first 32, later dS^T over
-      // the last 32), so the groups never touch each other's columns.
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int ch = 2 * half + cc;
+      {
+        // P^T = exp2(S^T scale log2e - LSE log2e) -> bf16 pairs
         uint32_t sv[32];
-        tmem_ld32(t_s + 32 * ch, sv);
-        float lv[32];
-#pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 x = reinterpret_cast<const float4*>(lse2 + 32 * ch)[k4];
-          lv[4 * k4] = x.x; lv[4 * k4 + 1] = x.y; lv[4 * k4 + 2] = x.z; lv[4 * k4 + 3] = x.w;
-        }
+        tmem_ld32(t_s, sv);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
+          const float2 l = reinterpret_cast<const float2*>(lse2)[k];
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
-                                    sc2, f2_pack(-lv[2 * k], -lv[2 * k + 1]));
+                                    sc2, f2_pack(-l.x, -l.y));
           float x0, x1;
           f2_unpack(x, x0, x1);
           float p0 = ex2(x0), p1 = ex2(x1);
           if (masked) {
-            const int i0 = qs.lo + (32 * ch + 2 * k) * qs.step;
+            const int i0 = i_first + 2 * k * qs.step;
             const int i1 = i0 + qs.step;
             if (i0 < cm.lo || i0 > cm.hi) p0 = 0.f;
             if (i1 < cm.lo || i1 > cm.hi) p1 = 0.f;
           }
           pk[k] = pack_bf16(p0, p1);
         }
-        tmem_st16(t_s + 64 * half + 16 * cc, pk);  // own columns, already read
+        tmem_st16(t_s, pk);  // own columns, already read
       }
       // P^T is in tensor memory: dV may start
       tmem_wait_st();
@@ -440,42 +442,31 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (ok && c > 0) ok = mbar_wait(bar(L::kDSFree), (c - 1) & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      tmem_wait_st();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int ch = 2 * half + cc;
+      {
+        // dS^T = P^T (dP^T - Delta)
         uint32_t dv[32], pv[16];
-        tmem_ld32(t_dp + 32 * ch, dv);
-        tmem_ld16(t_s + 64 * half + 16 * cc, pv);
-        float dl[32];
-#pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 x = reinterpret_cast<const float4*>(delta + 32 * ch)[k4];
-          dl[4 * k4] = x.x; dl[4 * k4 + 1] = x.y; dl[4 * k4 + 2] = x.z; dl[4 * k4 + 3] = x.w;
-        }
+        tmem_ld32(t_dp, dv);
+        tmem_ld16(t_s, pv);
         tmem_wait_ld();
-        uint32_t dk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
+          const float2 dl = reinterpret_cast<const float2*>(delta)[k];
           __nv_bfloat162 pp = *reinterpret_cast<__nv_bfloat162*>(&pv[k]);
           const float2 pf = __bfloat1622float2(pp);
           // dS = P dP - P Delta on packed pairs
           const uint64_t p2 = f2_pack(pf.x, pf.y);
           const uint64_t ds2 = f2_fma(p2, f2_pack(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1])),
-                                      f2_pack(-pf.x * dl[2 * k], -pf.y * dl[2 * k + 1]));
+                                      f2_pack(-pf.x * dl.x, -pf.y * dl.y));
           float d0, d1;
           f2_unpack(ds2, d0, d1);
-          dk[k] = pack_bf16(d0, d1);
+          pv[k] = pack_bf16(d0, d1);
         }
-        tmem_st16(t_s + 64 * half + 32 + 16 * cc, dk);  // own dead S^T columns
-        // dS (queries contiguous) into the 128B-swizzled MN-major tile:
-        // queries 32ch .. 32ch+31 are 16B chunks 4ch .. 4ch+3 of row j.
+        tmem_st16(t_s + 16, pv);  // own dead S^T columns
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int c8 = 4 * ch + q;  // 8-query chunk index (0..15)
-          const int mh = c8 >> 3, chunk = c8 & 7;
-          uint4 w = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
-          *reinterpret_cast<uint4*>(ds_row + mh * L::kHalfBytes + ((chunk ^ (j & 7)) << 4)) = w;
+          const int chunk = (4 * ch + q) & 7;
+          uint4 w = make_uint4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (j & 7)) << 4)) = w;
         }
       }
       tmem_wait_st();
@@ -485,20 +476,20 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) mbar_arrive(bar(L::kDSFull));
       ++c;
     }
-    // epilogue: group 0 writes dV, group 1 writes scale * dK for its key
+    // epilogue: warps 0-3 write dV, warps 4-7 scale * dK for their key
     // row, staged in the 128-byte swizzle in the V / K tile (free: every MMA
     // has completed) and stored with TMA by one thread of the group
-    if (ok) ok = mbar_wait(bar(L::kDKVFull), 0, abort_flag, P.status);
+    if (ok && half < 2) ok = mbar_wait(bar(L::kDKVFull), 0, abort_flag, P.status);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    if (ok) {
+    if (ok && half < 2) {
       uint8_t* stage = sm + (half ? L::kK : L::kV);
       const uint32_t src = tmem + lane_off + 256 + half * D;
       const float mul = half ? P.scale : 1.f;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int cq = 0; cq < D / 32; ++cq) {
         uint32_t o[32];
-        tmem_ld32(src + 32 * ch, o);
+        tmem_ld32(src + 32 * cq, o);
         tmem_wait_ld();
         uint32_t wp[16];
 #pragma unroll
@@ -507,10 +498,10 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           const float b = c > 0 ? __uint_as_float(o[2 * k + 1]) * mul : 0.f;
           wp[k] = pack_bf16(a, b);
         }
-        // columns 32 ch .. 32 ch + 31 = 16-byte chunks 4 ch .. 4 ch + 3
+        // columns 32 cq .. 32 cq + 31 = 16-byte chunks 4 cq .. 4 cq + 3
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int c8 = 4 * ch + q, hf = c8 >> 3, chunk = c8 & 7;
+          const int c8 = 4 * cq + q, hf = c8 >> 3, chunk = c8 & 7;
           *reinterpret_cast<uint4*>(stage + hf * L::kHalfBytes + j * 128 +
                                     ((chunk ^ (j & 7)) << 4)) =
               make_uint4(wp[4 * q], wp[4 * q + 1], wp[4 * q + 2], wp[4 * q + 3]);
@@ -540,12 +531,6 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     auto group_sync = [&](int b, int use) -> bool {
       mbar_arrive(bar(b));
       return __all_sync(0xffffffffu, mbar_wait(bar(b), use & 1, abort_flag, P.status));
-    };
-    auto load_half = [&](int hf, uint32_t (&v)[64]) {
-      const uint32_t src = tmem + lane_off + 128 + 64 * hf;
-      tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_wait_ld();
     };
     // staging box cg (32 fp32 columns x 128 rows, 16 KB): the first two fill
     // the dS tile (32 KB), the rest the dO half of the tile's slot
@@ -586,22 +571,19 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       // can refill it as soon as the tile's dK MMA is done.
       const int slot = c & 1;
 #pragma unroll
-      for (int hf = 0; hf < D / 64; ++hf) {
-        uint32_t v[64];
-        load_half(hf, v);
-        if (hf + 1 == D / 64) release_tmem();
+      for (int cg = 0; cg < kBoxes; ++cg) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + 128 + 32 * cg, v);
+        tmem_wait_ld();
+        if (cg + 1 == kBoxes) release_tmem();
+        uint8_t* rowp = stage_box(slot, cg) + i * 128;
 #pragma unroll
-        for (int cgl = 0; cgl < 2; ++cgl) {
-          uint8_t* rowp = stage_box(slot, 2 * hf + cgl) + i * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int q = 8 * cgl + k;
-            const float4 x = make_float4(__uint_as_float(v[4 * q]) * P.scale,
-                                         __uint_as_float(v[4 * q + 1]) * P.scale,
-                                         __uint_as_float(v[4 * q + 2]) * P.scale,
-                                         __uint_as_float(v[4 * q + 3]) * P.scale);
-            *reinterpret_cast<float4*>(rowp + ((k ^ (i & 7)) << 4)) = x;
-          }
+        for (int k = 0; k < 8; ++k) {
+          const float4 x = make_float4(__uint_as_float(v[4 * k]) * P.scale,
+                                       __uint_as_float(v[4 * k + 1]) * P.scale,
+                                       __uint_as_float(v[4 * k + 2]) * P.scale,
+                                       __uint_as_float(v[4 * k + 3]) * P.scale);
+          *reinterpret_cast<float4*>(rowp + ((k ^ (i & 7)) << 4)) = x;
         }
       }
       // the staged rows are read next by the TMA unit (async proxy)
