@@ -152,7 +152,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   const int g = ord.unit / P.Bt, bt = ord.unit % P.Bt;
   const int kappa = (kt * kTile) / P.shard;  // ring rank owning the key tile
 
-  if (threadIdx.x == 0) {
+  // The producer thread sets up the barriers and starts the K and V tiles'
+  // load before the CTA-wide barrier, so the load overlaps the set-up.
+  if (warp == kProducerWarp && lane == 0) {
     mbar_init(bar(L::kKVFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kQFull + s), 1);
@@ -177,6 +179,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kKVStaged + s), kTile / 32);
     *abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch(&tm_q);
+    tma_prefetch(&tm_k);
+    tma_prefetch(&tm_v);
+    tma_prefetch(&tm_do);
+    mbar_expect_tx(bar(L::kKVFull), 2 * L::kTileBytes);
+    for (int hf = 0; hf < L::kHalves; ++hf) {
+      tma_load_4d(sbase + L::kK + hf * L::kHalfBytes, &tm_k, bar(L::kKVFull), hf * 64, g,
+                  kt * kTile, bt);
+      tma_load_4d(sbase + L::kV + hf * L::kHalfBytes, &tm_v, bar(L::kKVFull), hf * 64, g,
+                  kt * kTile, bt);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(sbase + L::kMisc, 512);
@@ -190,19 +203,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch(&tm_q);
-      tma_prefetch(&tm_k);
-      tma_prefetch(&tm_v);
-      tma_prefetch(&tm_do);
       const TileSpan ks = tile_span(P, kt * kTile);
       const PosRange wq = query_window(P, ks);
-      mbar_expect_tx(bar(L::kKVFull), 2 * L::kTileBytes);
-      for (int hf = 0; hf < L::kHalves; ++hf) {
-        tma_load_4d(sbase + L::kK + hf * L::kHalfBytes, &tm_k, bar(L::kKVFull), hf * 64, g,
-                    kt * kTile, bt);
-        tma_load_4d(sbase + L::kV + hf * L::kHalfBytes, &tm_v, bar(L::kKVFull), hf * 64, g,
-                    kt * kTile, bt);
-      }
       int n = 0;    // tiles with Q and dO issued
       int nq = 0;   // tiles with Q issued (n or n + 1)
       bool ok = true;

@@ -121,7 +121,9 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   const int qbase0 = pair * 2 * kBM;          // permuted row of tile 0
   const int rho = qbase0 / P.shard;           // ring rank of both tiles
 
-  if (threadIdx.x == 0) {
+  // The producer thread sets up the barriers and starts the query tiles'
+  // load before the CTA-wide barrier, so the load overlaps the set-up.
+  if (warp == kProducerWarp && lane == 0) {
     mbar_init(bar(L::kQFull), 1);
     for (int s = 0; s < kVSlots; ++s) {
       mbar_init(bar(L::kVFull + s), 1);
@@ -139,6 +141,14 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kMmaDone), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch(&tm_q);
+    tma_prefetch(&tm_k);
+    tma_prefetch(&tm_v);
+    mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
+    for (int i = 0; i < 2; ++i)
+      for (int hf = 0; hf < L::kHalves; ++hf)
+        tma_load_4d(sbase + L::kQ + i * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
+                    bar(L::kQFull), hf * 64, h, qbase0 + i * kBM, bt);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(sbase + L::kMisc, 512);
@@ -152,18 +162,10 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch(&tm_q);
-      tma_prefetch(&tm_k);
-      tma_prefetch(&tm_v);
       const TileSpan q0 = tile_span(P, qbase0), q1 = tile_span(P, qbase0 + kBM);
       const KeyWindows w0 = key_windows(P, q0), w1 = key_windows(P, q1);
       const PosRange band = {min(w0.band.lo, w1.band.lo), max(w0.band.hi, w1.band.hi)};
       const PosRange sinks = {min(w0.sink.lo, w1.sink.lo), max(w0.sink.hi, w1.sink.hi)};
-      mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
-      for (int i = 0; i < 2; ++i)
-        for (int hf = 0; hf < L::kHalves; ++hf)
-          tma_load_4d(sbase + L::kQ + i * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
-                      bar(L::kQFull), hf * 64, h, qbase0 + i * kBM, bt);
       int n = 0;   // key tiles with K and V issued
       int nk = 0;  // key tiles with K issued (n or n + 1)
       bool ok = true;
@@ -464,11 +466,14 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     if (ok) {
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       uint8_t* stage = sm + L::kQ + i * L::kTileBytes;
+      // all of O's columns in one round trip to tensor memory
+      uint32_t ov[D / 32][32];
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(o_tm + 32 * ch, ov[ch]);
+      tmem_wait_ld();
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(o_tm + 32 * ch, o);
-        tmem_wait_ld();
+        const uint32_t* o = ov[ch];
         uint32_t wp[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
