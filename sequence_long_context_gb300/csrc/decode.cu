@@ -14,8 +14,9 @@
 //
 // HBM-bound: every cached key and value is read once. A CTA (one per SM)
 // streams its piece through shared memory in tiles of 64 keys (TMA, 128-byte
-// swizzle, five stages filled by a producer warp). Tile i belongs to the
-// pair of compute warps i mod 5, each taking 32 of its keys; every warp runs its
+// swizzle, six stages for up to four query rows per KV head, else five,
+// filled by a producer warp). Tile i belongs to the pair of compute warps
+// i mod stages, each taking 32 of its keys; every warp runs its
 // own online softmax over its keys, so no block-wide barrier is needed
 // inside the loop:
 //   scores   a lane pair per key, each lane of the pair takes half of D and
@@ -44,11 +45,17 @@ __device__ int g_decode_status = 0;
 
 constexpr int kKeys = 64;           // keys per tile
 constexpr int kMaxRows = 16;        // G * Tq
-constexpr int kStages = 5;          // K/V tiles in flight per CTA (one CTA per SM)
 constexpr int kWarpsPerTile = 2;    // a tile's keys are split between two warps
 constexpr int kWarpKeys = kKeys / kWarpsPerTile;
-constexpr int kComputeWarps = kStages * kWarpsPerTile;
-constexpr int kThreads = 32 * (kComputeWarps + 1);  // + one producer warp
+
+// K/V tiles in flight per CTA (one CTA per SM), and so compute warps. With
+// at most four query rows per KV head the rows' accumulators leave room for
+// six stages (thirteen warps: four share a 16K-register sub-partition, so
+// <= 128 registers each); with more rows five (eleven warps, <= 168).
+template <int R>
+__host__ __device__ constexpr int stages_for() { return R <= 4 ? 6 : 5; }
+template <int R>
+__host__ __device__ constexpr int threads_for() { return 32 * (stages_for<R>() * kWarpsPerTile + 1); }
 
 // keys scored together by a lane pair (sharing each chunk of q): both of
 // its keys, or one when the rows' accumulators would not fit the registers
@@ -78,6 +85,9 @@ __device__ __forceinline__ int q_index(int r, int d) {
 
 template <int D, int R>
 struct DSmem {
+  static constexpr int kStages = stages_for<R>();
+  static constexpr int kComputeWarps = kStages * kWarpsPerTile;
+  static constexpr int kThreads = threads_for<R>();  // + one producer warp
   static constexpr int kTileBytes = kKeys * D * 2;  // one K or V tile
   static constexpr int kBoxBytes = kKeys * 128;     // 64 columns x 64 keys
   static constexpr int kK = 0;                      // kStages stages
@@ -112,10 +122,11 @@ __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
 // R: query rows per KV head, padded to a compiled size (rows >= P.R are
 // zero queries whose results are never written).
 template <int D, int R>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(threads_for<R>())
 decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v) {
   using L = DSmem<D, R>;
+  constexpr int kStages = L::kStages, kComputeWarps = L::kComputeWarps, kThreads = L::kThreads;
   static_assert(R <= kMaxRows, "rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -186,7 +197,7 @@ decode_split_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tm
   } else {
     // ---------------------------------------------------------- compute warps
     // Each warp runs its own online softmax over its keys of its tiles
-    // (tiles i = warp / 2, warp / 2 + 5, ..., keys [32 h, 32 h + 32) with
+    // (tiles i = warp / 2, warp / 2 + stages, ..., keys [32 h, 32 h + 32) with
     // h = warp mod 2): running max m, running sum l and the O accumulator
     // (packed fp32 pairs, lane owns columns kCols*lane ..), merged across
     // warps at the end.
@@ -434,22 +445,22 @@ usp_status_t launch_d(const DecodeParams& P, const void* k, const void* v, cudaS
   DecodeParams Pk = P;
   Pk.status = status;
   dim3 grid(P.Hkv, P.n_part, P.B);
-  auto go = [&](auto kernel, int smem) -> usp_status_t {
+  auto go = [&](auto kernel, int smem, int threads) -> usp_status_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smem);
     if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(smem)", e);
     {
       ProfScope ps(st, "attn_decode_split");
-      kernel<<<grid, kThreads, smem, st>>>(Pk, mk, mv);
+      kernel<<<grid, threads, smem, st>>>(Pk, mk, mv);
     }
     note_launch();
     return check_launch();
   };
-  if (P.R <= 1) return go(decode_split_kernel<D, 1>, DSmem<D, 1>::kAlloc);
-  if (P.R <= 2) return go(decode_split_kernel<D, 2>, DSmem<D, 2>::kAlloc);
-  if (P.R <= 4) return go(decode_split_kernel<D, 4>, DSmem<D, 4>::kAlloc);
-  if (P.R <= 8) return go(decode_split_kernel<D, 8>, DSmem<D, 8>::kAlloc);
-  return go(decode_split_kernel<D, 16>, DSmem<D, 16>::kAlloc);
+  if (P.R <= 1) return go(decode_split_kernel<D, 1>, DSmem<D, 1>::kAlloc, DSmem<D, 1>::kThreads);
+  if (P.R <= 2) return go(decode_split_kernel<D, 2>, DSmem<D, 2>::kAlloc, DSmem<D, 2>::kThreads);
+  if (P.R <= 4) return go(decode_split_kernel<D, 4>, DSmem<D, 4>::kAlloc, DSmem<D, 4>::kThreads);
+  if (P.R <= 8) return go(decode_split_kernel<D, 8>, DSmem<D, 8>::kAlloc, DSmem<D, 8>::kThreads);
+  return go(decode_split_kernel<D, 16>, DSmem<D, 16>::kAlloc, DSmem<D, 16>::kThreads);
 }
 
 }  // namespace
