@@ -111,14 +111,18 @@ typedef enum {
  * order; lse stays rank-major (it is the forward's state for the backward).
  * The result equals extracting the inputs (USP_PERMUTE_EXTRACT), calling
  * without the flag and restoring the outputs (USP_PERMUTE_RESTORE), bit for
- * bit. With ulysses_degree > 1 the extract and restore ride along with the
- * Ulysses exchange, so each tensor is moved once instead of twice; with
- * ulysses_degree == 1 the kernels work on rank-major copies in the
- * workspace (usp_attn_*_workspace_size must be given the flag). Combined
- * with USP_FLAG_SAVED_EXCHANGE the backward also reuses those copies of
- * q, k, v, out at ulysses_degree == 1. Not supported by the q/k/v-packed
- * entry points and usp_attn_fwd_fp8 (USP_ERR_UNSUPPORTED). Forward and
- * backward must be given the same flags. */
+ * bit (dq to rounding: its additions happen in hardware order). Where the
+ * tensor-core kernels run and the layout is contiguous or zigzag, they read
+ * and write the caller's tensors in place (a 128-token tile is then a run of
+ * natural positions), with no copy at all. Otherwise (stripe, the CUDA-core
+ * kernels) the extract and restore ride along with the Ulysses exchange
+ * when ulysses_degree > 1, or run as copies into the workspace when
+ * ulysses_degree == 1 (usp_attn_*_workspace_size must be given the flag).
+ * q, k, v, out must be passed to the backward even with
+ * USP_FLAG_SAVED_EXCHANGE (which then only spares the copy path's copies).
+ * Not supported by the q/k/v-packed entry points and usp_attn_fwd_fp8
+ * (USP_ERR_UNSUPPORTED). Forward and backward must be given the same
+ * flags. */
 #define USP_FLAG_NATURAL_ORDER 4u
 
 /*

@@ -227,6 +227,20 @@ Shape shape_of(int B, int S, int Hq, int Hkv, int D, int cp, int ud,
   return s;
 }
 
+// Parameters of a natural-order call run in place: every head of the
+// caller's tensors is attended as it stands. Attention is per head, so the
+// Ulysses head groups (a batch view of the exchanged tensors) are not
+// formed: one group of all heads, whose [B][S][H][D] tensors differ from the
+// kernels' own layout only by the order of their rows.
+AttnParams inplace_params(const Shape& s, float scale, int causal, int window, int sink,
+                          const int32_t* cu) {
+  Shape one = s;
+  one.ud = 1;
+  AttnParams P = make_params(one, scale, causal, window, sink, cu);
+  P.nat = 1;
+  return P;
+}
+
 bool use_tc_fwd(const AttnParams& P, const Shape& s, unsigned flags) {
   return s.dtype == USP_BF16 && !(flags & USP_FLAG_FORCE_SIMT) &&
          fwd_tc_supported(P);
@@ -382,7 +396,14 @@ usp_status_t attn_fwd_impl(const void* q, const void* k, const void* v,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   AttnParams P = make_params(s, softmax_scale, causal, window, sink_tokens,
                              cu_seqlens);
-  if (s.ud > 1 && !s.natural) {
+  // natural-order tensors read and written in place by the tensor-core
+  // kernel (its 128-row tiles are runs of natural rows except for stripe)
+  const bool inplace = s.natural && s.layout != USP_LAYOUT_STRIPE && tok == 0 &&
+                       use_tc_fwd(P, s, flags);
+  if (inplace) {
+    P = inplace_params(s, softmax_scale, causal, window, sink_tokens, cu_seqlens);
+    P.q = q; P.k = k; P.v = v; P.o = out;
+  } else if (s.ud > 1 && !s.natural) {
     if ((r = a2a(q, w.q, s, Hq, 1, st, tok)) != USP_OK) return r;
     if ((r = a2a(k, w.k, s, Hkv, 1, st, tok)) != USP_OK) return r;
     if ((r = a2a(v, w.v, s, Hkv, 1, st, tok)) != USP_OK) return r;
@@ -402,7 +423,7 @@ usp_status_t attn_fwd_impl(const void* q, const void* k, const void* v,
   else
     r = launch_fwd_simt(P, dtype == USP_BF16, st);
   if (r != USP_OK) return r;
-  if (s.staged()) r = stage(w.o, out, s, Hq, 0, st);
+  if (s.staged() && !inplace) r = stage(w.o, out, s, Hq, 0, st);
   return r;
 }
 
@@ -456,7 +477,9 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
   // saved: the workspace holds the forward's copies of q, k, v, out (head
   // groups, or rank-major copies of natural-order tensors)
   const bool saved = (flags & USP_FLAG_SAVED_EXCHANGE) && s.staged();
-  if (S > 0 && (!lse || !dout || !dq || !dk || !dv || (!saved && (!q || !k || !v || !out))))
+  // natural-order calls may read q, k, v, out in place, so they always need them
+  const bool need_qkvo = !saved || s.natural;
+  if (S > 0 && (!lse || !dout || !dq || !dk || !dv || (need_qkvo && (!q || !k || !v || !out))))
     return USP_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv, workspace};
   for (const void* p : ptrs)
@@ -469,7 +492,12 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
   Carve c(workspace);
   BwdWs w = carve_bwd(c, s, tc);
   if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
-  if (s.staged()) {
+  const bool inplace = s.natural && s.layout != USP_LAYOUT_STRIPE && tok == 0 && tc;
+  if (inplace) {
+    P = inplace_params(s, softmax_scale, causal, window, sink_tokens, cu_seqlens);
+    P.q = q; P.k = k; P.v = v; P.o = const_cast<void*>(out); P.dout = dout;
+    P.dq = dq; P.dk = dk; P.dv = dv;
+  } else if (s.staged()) {
     if (!saved) {
       if (s.natural) {
         if ((r = stage(q, w.q, s, Hq, 1, st)) != USP_OK) return r;
@@ -501,6 +529,7 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
   else
     r = launch_bwd_simt(P, dtype == USP_BF16, st);
   if (r != USP_OK) return r;
+  if (inplace) return USP_OK;
   if (s.ud > 1 && !s.natural) {
     if ((r = a2a(w.dq, dq, s, Hq, 0, st, tok)) != USP_OK) return r;
     if ((r = a2a(w.dk, dk, s, Hkv, 0, st, tok)) != USP_OK) return r;

@@ -184,11 +184,12 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     tma_prefetch(&tm_v);
     tma_prefetch(&tm_do);
     mbar_expect_tx(bar(L::kKVFull), 2 * L::kTileBytes);
+    const TensorPos kv = tensor_pos(P, g, kt * kTile, bt, P.Hkv);
     for (int hf = 0; hf < L::kHalves; ++hf) {
-      tma_load_4d(sbase + L::kK + hf * L::kHalfBytes, &tm_k, bar(L::kKVFull), hf * 64, g,
-                  kt * kTile, bt);
-      tma_load_4d(sbase + L::kV + hf * L::kHalfBytes, &tm_v, bar(L::kKVFull), hf * 64, g,
-                  kt * kTile, bt);
+      tma_load_4d(sbase + L::kK + hf * L::kHalfBytes, &tm_k, bar(L::kKVFull), hf * 64, kv.h,
+                  kv.row, kv.b);
+      tma_load_4d(sbase + L::kV + hf * L::kHalfBytes, &tm_v, bar(L::kKVFull), hf * 64, kv.h,
+                  kv.row, kv.b);
     }
   }
   if (warp == kMmaWarp) {
@@ -241,9 +242,10 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
               bulk_load(st, P.lse2 + row_off, kTile * 4, bar(L::kQFull + slot));
               bulk_load(st + kTile * 4, P.delta + row_off, kTile * 4, bar(L::kQFull + slot));
             }
+            const TensorPos qp = tensor_pos(P, h, qt * kTile, bt, P.Hq);
             for (int hf = 0; hf < L::kHalves; ++hf)
               tma_load_4d(sbase + L::kQ + slot * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
-                          bar(L::kQFull + slot), hf * 64, h, qt * kTile, bt);
+                          bar(L::kQFull + slot), hf * 64, qp.h, qp.row, qp.b);
             ++nq;
             if (use >= 1 && !(ok = mbar_wait(bar(L::kStageFreeDO + slot), (use - 1) & 1,
                                              abort_flag, P.status)))
@@ -251,7 +253,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
             mbar_expect_tx(bar(L::kDOFull + slot), L::kTileBytes);
             for (int hf = 0; hf < L::kHalves; ++hf)
               tma_load_4d(sbase + L::kDO + slot * L::kTileBytes + hf * L::kHalfBytes, &tm_do,
-                          bar(L::kDOFull + slot), hf * 64, h, qt * kTile, bt);
+                          bar(L::kDOFull + slot), hf * 64, qp.h, qp.row, qp.b);
             ++n;
           }
         }
@@ -514,9 +516,10 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) mbar_arrive(bar(L::kKVStaged + half));
       if (quarter == 0 && lane == 0 &&
           mbar_wait(bar(L::kKVStaged + half), 0, abort_flag, P.status)) {
+        const TensorPos kv = tensor_pos(P, g, kt * kTile, bt, P.Hkv);
         for (int hf = 0; hf < L::kHalves; ++hf)
           tma_store_4d(half ? &tm_dk : &tm_dv, smem_u32(stage + hf * L::kHalfBytes), hf * 64,
-                       g, kt * kTile, bt);
+                       kv.h, kv.row, kv.b);
         bulk_commit_group();
         // the tile has been read out of shared memory before the CTA exits
         // (the global writes complete on their own)
@@ -624,15 +627,24 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
 
 // dq (bf16) <- dq_acc (fp32), 8 elements per thread-iteration. Token rows of
 // row8 8-element groups; dst rows are tok8 groups apart (== row8 when dense,
-// three times it in a packed q/k/v gradient).
+// three times it in a packed q/k/v gradient). With P.nat the dst is the
+// caller's natural-order dq: head group u of token row p goes to groups
+// u*row8.. of natural row nat(p), rows tok8 = ud*row8 apart.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src,
                                                          uint4* __restrict__ dst,
                                                          long long n8, int row8,
-                                                         long long tok8) {
+                                                         long long tok8, const AttnParams P) {
   for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n8; i += (long long)gridDim.x * 256) {
     const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
     const long long row = i / row8;
-    dst[row * tok8 + (i - row * row8)] =
+    long long drow = row, doff = 0;
+    if (P.nat) {
+      const int bt = (int)(row / P.S), p = (int)(row - (long long)bt * P.S);
+      const int u = bt / P.B;
+      drow = (long long)(bt - u * P.B) * P.S + nat_pos(p, P.layout, P.cp, P.shard, P.chunk);
+      doff = (long long)u * row8;
+    }
+    dst[drow * tok8 + doff + (i - row * row8)] =
         make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
                    pack_bf16(b.z, b.w));
   }
@@ -685,13 +697,16 @@ template <int D>
 usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   const long long tok = P.qkv_tok;
-  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D, false, tok) ||
-      !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D, false, tok) ||
-      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D, false, tok) ||
-      !make_map(&mdo, P.dout, P.Bt, P.S, P.Hq, D) ||
+  // natural-order tensors in place: all heads of every token, B batch rows
+  // (the dQ accumulator stays in the kernels' own head groups)
+  const int Bm = P.nat ? P.B : P.Bt, hm = P.nat ? P.ud : 1;
+  if (!make_map(&mq, P.q, Bm, P.S, P.Hq * hm, D, false, tok) ||
+      !make_map(&mk, P.k, Bm, P.S, P.Hkv * hm, D, false, tok) ||
+      !make_map(&mv, P.v, Bm, P.S, P.Hkv * hm, D, false, tok) ||
+      !make_map(&mdo, P.dout, Bm, P.S, P.Hq * hm, D) ||
       !make_map(&mdq, P.dq_acc, P.Bt, P.S, P.Hq, D, true) ||
-      !make_map(&mdk, P.dk, P.Bt, P.S, P.Hkv, D, false, tok) ||
-      !make_map(&mdv, P.dv, P.Bt, P.S, P.Hkv, D, false, tok))
+      !make_map(&mdk, P.dk, Bm, P.S, P.Hkv * hm, D, false, tok) ||
+      !make_map(&mdv, P.dv, Bm, P.S, P.Hkv * hm, D, false, tok))
     return USP_ERR_CUDA;
   static int* status = nullptr;
   if (status == nullptr) {
@@ -741,7 +756,7 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
     dq_convert_kernel<<<(unsigned)(n8 < 152LL * 32 * 4 ? (n8 + 255) / 256 : 152 * 16), 256, 0,
                         st>>>(reinterpret_cast<const float4*>(P.dq_acc),
                               reinterpret_cast<uint4*>(P.dq), n8, P.Hq * D / 8,
-                              qkv_stride(P, P.Hq) / 8);
+                              P.nat ? (long long)P.ud * P.Hq * D / 8 : qkv_stride(P, P.Hq) / 8, P);
   }
   note_launch();
   return check_launch();

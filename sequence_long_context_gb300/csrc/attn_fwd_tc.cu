@@ -145,10 +145,12 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     tma_prefetch(&tm_k);
     tma_prefetch(&tm_v);
     mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 2; ++i) {
+      const TensorPos t = tensor_pos(P, h, qbase0 + i * kBM, bt, P.Hq);
       for (int hf = 0; hf < L::kHalves; ++hf)
         tma_load_4d(sbase + L::kQ + i * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
-                    bar(L::kQFull), hf * 64, h, qbase0 + i * kBM, bt);
+                    bar(L::kQFull), hf * 64, t.h, t.row, t.b);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(sbase + L::kMisc, 512);
@@ -190,10 +192,11 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                                          abort_flag, P.status)))
           return;
         sched[slot] = make_int4(kt, c0, c1, 0);
+        const TensorPos kv = tensor_pos(P, g, kt * kBN, bt, P.Hkv);
         mbar_expect_tx(bar(L::kKFull + slot), L::kTileBytes);
         for (int hf = 0; hf < L::kHalves; ++hf)
           tma_load_4d(sbase + L::kK + slot * L::kTileBytes + hf * L::kHalfBytes,
-                      &tm_k, bar(L::kKFull + slot), hf * 64, g, kt * kBN, bt);
+                      &tm_k, bar(L::kKFull + slot), hf * 64, kv.h, kv.row, kv.b);
         ++nk;
         const int vslot = n % kVSlots, vuse = n / kVSlots;
         if (vuse >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + vslot), (vuse - 1) & 1,
@@ -202,7 +205,7 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         mbar_expect_tx(bar(L::kVFull + vslot), L::kTileBytes);
         for (int hf = 0; hf < L::kHalves; ++hf)
           tma_load_4d(sbase + L::kV + vslot * L::kTileBytes + hf * L::kHalfBytes,
-                      &tm_v, bar(L::kVFull + vslot), hf * 64, g, kt * kBN, bt);
+                      &tm_v, bar(L::kVFull + vslot), hf * 64, kv.h, kv.row, kv.b);
         ++n;
       };
       for (int s = 0; s < P.cp && ok; ++s) {
@@ -496,9 +499,10 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) mbar_arrive(bar(L::kOStaged + i));
       if (quarter == 0 && lane == 0) {
         if (mbar_wait(bar(L::kOStaged + i), 0, abort_flag, P.status)) {
+          const TensorPos t = tensor_pos(P, h, qbase0 + i * kBM, bt, P.Hq);
           for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_store_4d(&tm_o, smem_u32(stage + hf * L::kHalfBytes), hf * 64, h,
-                         qbase0 + i * kBM, bt);
+            tma_store_4d(&tm_o, smem_u32(stage + hf * L::kHalfBytes), hf * 64, t.h, t.row,
+                         t.b);
           bulk_commit_group();
           // the tile has been read out of shared memory before the CTA exits
           // (the global writes complete on their own)
@@ -560,10 +564,12 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
 template <int D>
 usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, P.q, P.Bt, P.S, P.Hq, D, P.qkv_tok) ||
-      !make_map(&mk, P.k, P.Bt, P.S, P.Hkv, D, P.qkv_tok) ||
-      !make_map(&mv, P.v, P.Bt, P.S, P.Hkv, D, P.qkv_tok) ||
-      !make_map(&mo, P.o, P.Bt, P.S, P.Hq, D))
+  // natural-order tensors in place: all heads of every token, B batch rows
+  const int Bm = P.nat ? P.B : P.Bt, hm = P.nat ? P.ud : 1;
+  if (!make_map(&mq, P.q, Bm, P.S, P.Hq * hm, D, P.qkv_tok) ||
+      !make_map(&mk, P.k, Bm, P.S, P.Hkv * hm, D, P.qkv_tok) ||
+      !make_map(&mv, P.v, Bm, P.S, P.Hkv * hm, D, P.qkv_tok) ||
+      !make_map(&mo, P.o, Bm, P.S, P.Hq * hm, D))
     return USP_ERR_CUDA;  // detail recorded by make_map
   const int smem = Smem<D>::kAlloc;
   static int* status = nullptr;

@@ -136,8 +136,15 @@ bwd_preprocess_kernel(AttnParams P, int zero_dq) {
     const int p = (int)(bp % P.S);
     const int bt = (int)(bp / P.S);
     float o[E], d[E];
-    load_row<T, E>(reinterpret_cast<const T*>(P.o) + r * D + lane * E, o);
-    load_row<T, E>(reinterpret_cast<const T*>(P.dout) + r * D + lane * E, d);
+    // the caller's natural-order out and dout in place (tensor-core path),
+    // else the kernels' own [bt][p][h] rows
+    long long src = r;
+    if (P.nat) {
+      const TensorPos t = tensor_pos(P, h, p, bt, P.Hq);
+      src = ((long long)t.b * P.S + t.row) * ((long long)P.ud * P.Hq) + t.h;
+    }
+    load_row<T, E>(reinterpret_cast<const T*>(P.o) + src * D + lane * E, o);
+    load_row<T, E>(reinterpret_cast<const T*>(P.dout) + src * D + lane * E, d);
     float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) acc = fmaf(o[e], d[e], acc);

@@ -54,6 +54,11 @@ struct AttnParams {
   // elements between consecutive tokens of q, k, v, dq, dk, dv: 0 = dense
   // ([.., H, D] rows of H*D); 3*H*D for a packed [B, S, 3, H, D] tensor
   long long qkv_tok;
+  // 1: q, k, v, o, dout, dq, dk, dv are the caller's natural-order tensors
+  // [B][S][ud*H][D], read and written in place (tensor-core kernels, layouts
+  // whose 128-row tiles are runs of natural positions); 0: the kernels' own
+  // rank-major head groups [Bt][S][H][D]
+  int nat;
 };
 
 // Token stride of q/k/v/dq/dk/dv rows with H heads.
@@ -194,6 +199,22 @@ __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
+}
+
+// Where head h of head group bt (= u*B + b) at rank-major row p sits in a
+// q/k/v/o/dout-like tensor with H heads per group: (head, row, batch) of the
+// kernels' own layout, or with P.nat of the caller's natural-order tensor
+// (global head u*H + h, natural row). A 128-row tile of a contiguous or
+// zigzag layout is a run of natural rows, so a tile's first row gives its
+// TMA coordinate.
+struct TensorPos {
+  int h, row, b;
+};
+__host__ __device__ __forceinline__ TensorPos tensor_pos(const AttnParams& P, int h, int p,
+                                                         int bt, int H) {
+  if (!P.nat) return {h, p, bt};
+  const int u = bt / P.B;
+  return {u * H + h, nat_pos(p, P.layout, P.cp, P.shard, P.chunk), bt - u * P.B};
 }
 
 __host__ __device__ __forceinline__ long long lse_index(const AttnParams& P,

@@ -1,9 +1,11 @@
 """GPU parity of the natural-order calls (FLAG_NATURAL_ORDER): q, k, v, out,
-dout, dq, dk, dv in natural sequence order, with the layout's extract and
-restore done inside the call (fused into the Ulysses exchange when
-ulysses_degree > 1). The result must equal extracting the inputs, calling in
-rank-major order and restoring the outputs (YunChang README, "2. Usage":
-the inputs are reordered by the extract function before the attention):
+dout, dq, dk, dv in natural sequence order, read and written in place by the
+tensor-core kernels (contiguous and zigzag layouts), or with the layout's
+extract and restore done inside the call (stripe, the CUDA-core kernels:
+fused into the Ulysses exchange when ulysses_degree > 1). The result must
+equal extracting the inputs, calling in rank-major order and restoring the
+outputs (YunChang README, "2. Usage": the inputs are reordered by the
+extract function before the attention):
 out, lse, dk, dv bit for bit; dq is reduced in hardware order, so it is
 checked against the oracle."""
 import numpy as np
@@ -54,13 +56,10 @@ def test_natural_order_matches_extract_call_restore(case, saved):
     ws.fill_(0x7F)  # stale contents must not matter
     out, lse = usp.attn_forward(nat["q"], nat["k"], nat["v"], workspace=ws, natural=True, **kw)
     assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
-    if saved:  # the saved copies stand in for q, k, v, out
-        z = torch.zeros_like
-        args = (z(nat["q"]), z(nat["k"]), z(nat["v"]), z(out))
-    else:
-        args = (nat["q"], nat["k"], nat["v"], out)
-    grads = usp.attn_backward(*args, lse, nat["dout"], workspace=ws, natural=True,
-                              saved_exchange=saved, **kw)
+    # saved: the copy path reuses the forward's copies of q, k, v, out; the
+    # in-place path (tensor-core kernels, contiguous / zigzag) reads them
+    grads = usp.attn_backward(nat["q"], nat["k"], nat["v"], out, lse, nat["dout"], workspace=ws,
+                              natural=True, saved_exchange=saved, **kw)
     assert torch.equal(grads[1], unperm(ref_grads[1]))
     assert torch.equal(grads[2], unperm(ref_grads[2]))
     ref = attention.attn_bwd(x["q"], x["k"], x["v"], x["dout"], w.scale, w.causal, w.window,

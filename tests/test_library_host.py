@@ -275,9 +275,12 @@ def test_natural_order_flag_host_checks(lib):
     # ud = 1 with the flag: the call gets as far as the missing workspace
     assert fwd(lib, flags=N) == 4
     assert bwd(lib, ud=1, flags=N) == 4
-    # saved copies at ud = 1: q, k, v, out may be NULL
+    # natural-order backward calls may read q, k, v, out in place: they are
+    # needed even with the saved-exchange flag
     assert bwd(lib, ud=1, flags=N | usp.FLAG_SAVED_EXCHANGE, q=None, k=None, v=None,
-               out=None) == 4
+               out=None) == 1
+    assert bwd(lib, flags=N | usp.FLAG_SAVED_EXCHANGE, q=None, k=None, v=None,
+               out=None) == 1
     # the packed entry points and the e4m3 forward do not take it
     assert lib.usp_attn_fwd_qkvpacked(FAKE, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0, 0, None, 4,
                                       1, 1, 1, N, None, 0, None) == 2
