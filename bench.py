@@ -299,6 +299,44 @@ def make_step(usp, w, x, cu_dev, keep=None):
     return step
 
 
+def rank_major_kernels(usp, torch, w, x, cu_dev, F, steps, peak):
+    """The step's attention kernels on rank-major copies of the inputs (the
+    layout's extract done once, outside the timed loop; the Ulysses exchange
+    inside the calls as usual): each kernel's average CUDA-event time and
+    useful TFLOP/s against `peak`. The natural-order step above has the same
+    kernels read the caller's tensors in place."""
+    kw = dict(causal=w.causal, window=w.window, sink_tokens=w.sink_tokens,
+              cu_seqlens=cu_dev, cp=w.cp, ud=w.ud, layout=w.layout)
+    names = ["q", "k", "v"] + (["dout"] if w.backward else [])
+    xp = {n: usp.permute(x[n], "extract", w.layout, w.cp) for n in names}
+    ws = usp.attn_workspace(xp["q"], xp["k"], cu_seqlens=cu_dev, cp=w.cp, ud=w.ud)
+
+    def run():
+        o, l = usp.attn_forward(xp["q"], xp["k"], xp["v"], workspace=ws, **kw)
+        if w.backward:
+            usp.attn_backward(xp["q"], xp["k"], xp["v"], o, l, xp["dout"], workspace=ws,
+                              saved_exchange=True, **kw)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    usp.usp_profile_enable(True)
+    for _ in range(steps):
+        run()
+    torch.cuda.synchronize()
+    usp.usp_profile_enable(False)
+    ks = usp.usp_profile_read()
+    res = {"inputs": "rank-major copies (extract outside the timed loop)", "steps": steps}
+    for part, kname, work in (("fwd", "attn_fwd_tc", F["fwd"]), ("bwd", "attn_bwd_tc", F["bwd"])):
+        n, tot = ks.get(kname, (0, 0.0))
+        if n:
+            avg = tot / n
+            ach = work / (avg * 1e-3) / 1e12
+            res[part] = {"kernel": kname, "avg_ms": avg, "achieved": ach, "frac": ach / peak}
+    del xp, ws
+    return res
+
+
 def gate_point(usp, flops, torch, name, dev, seed, steps, warmup, pk, timed):
     """Forward and backward tensor-core kernels of one zigzag sweep point,
     each kernel's average CUDA-event time over `steps` training steps and its
@@ -451,6 +489,13 @@ def main():
             gbs = per_launch / (kernels[k]["avg_ms"] * 1e-3) / 1e9
             kernels[k].update({"bytes_per_launch": per_launch, "GB_s": gbs,
                                "frac_hbm": gbs / pk["hbm_gbs"]})
+
+    # the same attention kernels on rank-major copies of the step's inputs
+    try:
+        rank_major = rank_major_kernels(usp, torch, w, x, cu_dev, F, args.steps, tensor_peak)
+    except Exception as e:  # report, do not hide
+        rank_major = {"error": repr(e)}
+    torch.cuda.empty_cache()
 
     # standalone merge on its own workload (4 partials of B*S*Hq rows)
     merge_res = None
@@ -676,7 +721,8 @@ def main():
         "config": workload_config(w, F["total"], world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches * args.steps), "clocks": clocks,
-        "gate": gate, "kernels": kernels, "merge": merge_res, "decode": decode_res,
+        "gate": gate, "kernels": kernels, "kernels_rank_major": rank_major,
+        "merge": merge_res, "decode": decode_res,
         "fp8": fp8_res,
     }
     if rank == 0:
