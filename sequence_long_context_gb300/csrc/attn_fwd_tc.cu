@@ -522,8 +522,9 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
 
 // ---------------------------------------------------------------------------
 // One query tile per CTA, two CTAs per SM. For windowed problems (and
-// packed sequences) a query tile meets few key tiles, and a CTA's fixed costs (set-up, the Q load, the
-// first key tile, the epilogue) are a large share of its time. This variant
+// packed sequences) a query tile meets few key tiles, and a CTA's fixed
+// costs (set-up, the Q load, the first key tile, the epilogue) are a large
+// share of its time. This variant
 // takes half the tensor memory (S at [0,128), overwritten by P, O at
 // [128, 128+D)) and under half the shared memory (one Q tile, one K and one
 // V slot), so the SM runs two CTAs: one's start and end overlap the other's
