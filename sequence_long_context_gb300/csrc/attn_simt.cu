@@ -22,6 +22,8 @@
 // dQ rows are formed by one warp per query row over keys in ring order;
 // dK/dV rows by one warp per key row over every query rank that sees the
 // shard (the shard's ring return) and every query head of its GQA group.
+#include <type_traits>
+
 #include "internal.h"
 
 namespace usp {
@@ -159,6 +161,60 @@ bwd_preprocess_kernel(AttnParams P, int zero_dq) {
 #pragma unroll
       for (int e = 0; e < E; ++e) z[e] = 0.f;
       store_row<float, E>(P.dq_acc + r * D + lane * E, z);
+    }
+  }
+}
+
+// bf16 rows with 16-byte accesses: D/8 lanes per row (8 elements each), so
+// a warp covers 256/D rows per load instruction; the row's lanes reduce the
+// dot product among themselves. Same results and outputs as
+// bwd_preprocess_kernel.
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_preprocess_bf16_kernel(AttnParams P, int zero_dq) {
+  constexpr int kLanes = D / 8, kRowsPerWarp = 32 / kLanes;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % kLanes, grp = lane / kLanes;
+  const long long nrows = (long long)P.Bt * P.S * P.Hq;
+  const long long stride = (long long)gridDim.x * 8 * kRowsPerWarp;
+  for (long long r = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRowsPerWarp + grp;
+       r - grp < nrows; r += stride) {
+    const bool valid = r < nrows;
+    const int h = (int)(r % P.Hq);
+    const long long bp = r / P.Hq;
+    const int p = (int)(bp % P.S), bt = (int)(bp / P.S);
+    long long src = r;
+    if (P.nat) {
+      const TensorPos t = tensor_pos(P, h, p, bt, P.Hq);
+      src = ((long long)t.b * P.S + t.row) * ((long long)P.ud * P.Hq) + t.h;
+    }
+    float acc = 0.f;
+    if (valid) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(P.o) + src * D) + sub);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(P.dout) + src * D) + sub);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+        const float2 bf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
+        acc = fmaf(af.x, bf.x, acc);
+        acc = fmaf(af.y, bf.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (!valid) continue;
+    if (sub == 0) {
+      const long long di = ((long long)bt * P.Hq + h) * P.S + p;
+      P.delta[di] = acc;
+      if (P.lse2 != nullptr) P.lse2[di] = P.lse[lse_index(P, bt, h, p)] * kLog2e;
+    }
+    if (zero_dq) {
+      float4* z = reinterpret_cast<float4*>(P.dq_acc + r * D) + 2 * sub;
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
@@ -317,9 +373,14 @@ usp_status_t fwd_t(const AttnParams& P, cudaStream_t st) {
 template <typename T, int D>
 usp_status_t pre_t(const AttnParams& P, int zero, cudaStream_t st) {
   long long rows = (long long)P.Bt * P.S * P.Hq;
-  long long blocks = (rows + 7) / 8;
-  int grid = (int)(blocks < 152LL * 16 ? blocks : 152LL * 16);
-  {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    const long long blocks = (rows + 8 * (256 / D) - 1) / (8 * (256 / D));
+    const int grid = (int)(blocks < 152LL * 16 ? blocks : 152LL * 16);
+    ProfScope ps(st, "attn_bwd_preprocess");
+    bwd_preprocess_bf16_kernel<D><<<grid, 256, 0, st>>>(P, zero);
+  } else {
+    long long blocks = (rows + 7) / 8;
+    int grid = (int)(blocks < 152LL * 16 ? blocks : 152LL * 16);
     ProfScope ps(st, "attn_bwd_preprocess");
     bwd_preprocess_kernel<T, D><<<grid, 256, 0, st>>>(P, zero);
   }

@@ -63,6 +63,10 @@ def test_layouts_and_degrees(layout, cp, ud):
     dict(layout="contiguous", cp=4, S=1024, Hq=4, Hkv=4, window=200, sink_tokens=4),
     dict(layout="zigzag", cp=2, S=1024, Hq=4, Hkv=1, ud=1, causal=False),
     dict(layout="zigzag", cp=4, S=1024, Hq=4, Hkv=2, ud=2),
+    # windows through the one-tile-per-CTA forward, on every layout
+    dict(layout="stripe", cp=4, S=1024, Hq=4, Hkv=2, window=300),
+    dict(layout="zigzag", cp=2, S=1024, Hq=8, Hkv=2, window=250, sink_tokens=2),
+    dict(layout="zigzag", cp=2, S=1024, Hq=4, Hkv=2, ud=2, window=333),
 ])
 def test_bf16_d128(case, flags):
     w = BASE.replace(B=2, D=128, dtype="bf16", **case)
@@ -74,6 +78,21 @@ def test_bf16_d128(case, flags):
 def test_varlen(dtype, window, sink):
     w = BASE.replace(B=0, S=2048, Hq=4, Hkv=2, D=128, dtype=dtype, cp=8, layout="zigzag",
                      varlen=True, seg_lo=1, seg_hi=700, window=window, sink_tokens=sink)
+    check(w)
+
+
+@pytest.mark.parametrize("window,sink", [(0, 0), (400, 2)])
+def test_bf16_varlen_tensor_core(window, sink):
+    # 256-token zigzag chunks: the tensor-core kernels (the forward with one
+    # query tile per CTA) on a packed batch
+    w = BASE.replace(B=0, S=4096, Hq=4, Hkv=2, D=128, dtype="bf16", cp=8, layout="zigzag",
+                     varlen=True, seg_lo=100, seg_hi=1500, window=window, sink_tokens=sink)
+    check(w)
+
+
+def test_bf16_d64_window():
+    w = BASE.replace(B=2, S=1024, Hq=4, Hkv=2, D=64, dtype="bf16", cp=4, layout="contiguous",
+                     window=200)
     check(w)
 
 
