@@ -112,12 +112,15 @@ typedef enum {
  * The result equals extracting the inputs (USP_PERMUTE_EXTRACT), calling
  * without the flag and restoring the outputs (USP_PERMUTE_RESTORE), bit for
  * bit (dq to rounding: its additions happen in hardware order). Where the
- * tensor-core kernels run and the layout is contiguous or zigzag, they read
- * and write the caller's tensors in place (a 128-token tile is then a run of
- * natural positions), with no copy at all. Otherwise (stripe, the CUDA-core
- * kernels) the extract and restore ride along with the Ulysses exchange
- * when ulysses_degree > 1, or run as copies into the workspace when
- * ulysses_degree == 1 (usp_attn_*_workspace_size must be given the flag).
+ * tensor-core kernels run, the layout is contiguous or zigzag (a 128-token
+ * tile is then a run of natural positions) and the problem is short per
+ * token (a window, a packed batch, or S <= 16384), they read and write the
+ * caller's tensors in place, with no copy at all. Otherwise (longer dense
+ * sequences, where copies cost less than reading in place; stripe; the
+ * CUDA-core kernels) the extract and restore ride along with the Ulysses
+ * exchange when ulysses_degree > 1, or run as copies into the workspace
+ * when ulysses_degree == 1 (usp_attn_*_workspace_size must be given the
+ * flag).
  * q, k, v, out must be passed to the backward even with
  * USP_FLAG_SAVED_EXCHANGE (which then only spares the copy path's copies).
  * Not supported by the q/k/v-packed entry points and usp_attn_fwd_fp8

@@ -241,6 +241,20 @@ AttnParams inplace_params(const Shape& s, float scale, int causal, int window, i
   return P;
 }
 
+// Natural-order calls read and write the caller's tensors in place where a
+// 128-row tile is a run of natural rows (contiguous, zigzag) and the problem
+// is short per token: the kernels take 1-4 % longer on the caller's tensors
+// than on rank-major copies, which pays while the copies (linear in the
+// sequence) cost more than that share of the attention (quadratic): windows,
+// packed batches (sequences of at most a few 10K tokens) and dense
+// sequences up to 16K tokens (measured: S=8K in place saves 0.07 ms of
+// 1.9, S=32K loses 0.15 ms of 26.5). The rule depends only on the call's
+// arguments, so forward and backward decide alike.
+bool natural_in_place(const Shape& s, int window, const int32_t* cu, long long tok) {
+  if (!s.natural || s.layout == USP_LAYOUT_STRIPE || tok != 0) return false;
+  return window > 0 || cu != nullptr || s.S <= 16384;
+}
+
 bool use_tc_fwd(const AttnParams& P, const Shape& s, unsigned flags) {
   return s.dtype == USP_BF16 && !(flags & USP_FLAG_FORCE_SIMT) &&
          fwd_tc_supported(P);
@@ -398,8 +412,7 @@ usp_status_t attn_fwd_impl(const void* q, const void* k, const void* v,
                              cu_seqlens);
   // natural-order tensors read and written in place by the tensor-core
   // kernel (its 128-row tiles are runs of natural rows except for stripe)
-  const bool inplace = s.natural && s.layout != USP_LAYOUT_STRIPE && tok == 0 &&
-                       use_tc_fwd(P, s, flags);
+  const bool inplace = natural_in_place(s, window, cu_seqlens, tok) && use_tc_fwd(P, s, flags);
   if (inplace) {
     P = inplace_params(s, softmax_scale, causal, window, sink_tokens, cu_seqlens);
     P.q = q; P.k = k; P.v = v; P.o = out;
@@ -492,7 +505,7 @@ usp_status_t attn_bwd_impl(const void* q, const void* k, const void* v,
   Carve c(workspace);
   BwdWs w = carve_bwd(c, s, tc);
   if (!workspace || workspace_bytes < c.used) return USP_ERR_WORKSPACE;
-  const bool inplace = s.natural && s.layout != USP_LAYOUT_STRIPE && tok == 0 && tc;
+  const bool inplace = natural_in_place(s, window, cu_seqlens, tok) && tc;
   if (inplace) {
     P = inplace_params(s, softmax_scale, causal, window, sink_tokens, cu_seqlens);
     P.q = q; P.k = k; P.v = v; P.o = const_cast<void*>(out); P.dout = dout;
