@@ -94,6 +94,185 @@ __device__ __forceinline__ int fwd_batch(const AttnParams& P, int unit) {
   return (unit / P.G) % P.Bt;
 }
 
+// The softmax and epilogue of one query tile, one row per thread of four
+// warps (the row's TMEM lane quarter = warp % 4). Per key tile: P =
+// 2^(S scale log2e - m) written over S as bf16 pairs (the A operand of P V),
+// the running max m moved only when it grows by more than 2^8 (and O
+// rescaled then; exact, since O / l and m + log l do not depend on which m
+// was used), the row sum accumulated on packed pairs. Epilogue: O / l as
+// bf16 rows staged in `stage` (128-byte swizzle) and stored with TMA by the
+// first thread, LSE = (m + log2 l) ln 2. b_* are the tile's barriers;
+// nranks is the CTA order's ranks per unit (to recompute the head late).
+template <int D, int kHalfBytes, int kHalves>
+__device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* info,
+                                             uint32_t b_info, uint32_t b_s, uint32_t b_p,
+                                             uint32_t b_o, uint32_t b_staged, uint32_t s_tm,
+                                             uint32_t o_tm, uint8_t* stage,
+                                             const CUtensorMap* tm_o, int qrow0, int quarter,
+                                             int lane, int nranks, volatile int* abort_flag) {
+  const int r = quarter * 32 + lane;       // row within the tile = TMEM lane
+  const int prow = qrow0 + r;              // permuted query row
+  const RowMask rm = row_mask(P, nat_pos(P, prow));
+  float m_run = -INFINITY, l_run = 0.f;
+  int c = 0;
+  bool ok = true;
+  while (true) {
+    ok = mbar_wait(b_info, c & 1, abort_flag, P.status);
+    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+    const int2 inf = *info;
+    if (inf.x == kEnd) break;
+    // a masked tile: this row's visible keys in the tile (the main
+    // interval and the sink interval of row_visible) as one bit per column
+    uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+    if (inf.y == kMasked) {
+      const TileSpan ks = tile_span(P, inf.x * kBN);
+      const ColRange c0 = tile_cols(ks, rm.lo, rm.hi);
+      const ColRange c1 = tile_cols(ks, rm.qs, min(rm.sink_end - 1, rm.causal_hi));
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) vis[ch] = col_bits(c0, 32 * ch) | col_bits(c1, 32 * ch);
+    }
+    ok = mbar_wait(b_s, c & 1, abort_flag, P.status);
+    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+    tc_fence_after();
+    uint32_t sr[4][32];
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tm + 32 * ch, sr[ch]);
+    tmem_wait_ld();
+    if (inf.y == kMasked) {
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (!((vis[ch] >> j) & 1u)) sr[ch][j] = __float_as_uint(-INFINITY);
+    }
+    // row max as 8 independent chains (a single chain is latency-bound)
+    float m8[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[t >> 5][t & 31]);
+#pragma unroll
+    for (int j = 8; j < 128; ++j)
+      m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
+    float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+    mx *= P.scale_log2;
+    // lazy rescale: move the running max only when it grows by > 2^8
+    const bool need = mx > m_run + kRescaleThreshold;
+    float alpha = 1.f;
+    if (need) {
+      alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx);
+      m_run = mx;
+    }
+    l_run *= alpha;
+    const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+    // p = exp2(s * scale_log2 - m): scale-and-subtract and the row sum run
+    // on packed fp32 pairs (one FMA-pipe instruction per two elements)
+    const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
+    const uint64_t nm2 = f2_pack(-msub, -msub);
+    uint64_t ls2[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int j0 = 64 * ch + 2 * j;
+        const uint64_t x = f2_fma(
+            f2_pack(__uint_as_float(sr[j0 >> 5][j0 & 31]),
+                    __uint_as_float(sr[(j0 + 1) >> 5][(j0 + 1) & 31])),
+            sc2, nm2);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        ls2[j & 3] = f2_add(ls2[j & 3], f2_pack(p0, p1));
+        pk[j] = pack_bf16(p0, p1);
+      }
+      tmem_st32(s_tm + 32 * ch, pk);
+    }
+    {
+      float a0, a1, b0, b1, c0, c1, d0, d1;
+      f2_unpack(ls2[0], a0, a1);
+      f2_unpack(ls2[1], b0, b1);
+      f2_unpack(ls2[2], c0, c1);
+      f2_unpack(ls2[3], d0, d1);
+      l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+    }
+    // O_i holds PV of the previous tiles (complete: the commit that
+    // signalled S_i tracks every earlier MMA); rescale it to the new max
+    // before P_i V is accumulated onto it.
+    if (__any_sync(0xffffffffu, need && c > 0)) {
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(o_tm + 32 * ch, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+        tmem_st32(o_tm + 32 * ch, o);
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_p);  // one arrival per warp
+    ++c;
+  }
+  // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2. The rows are
+  // staged in the 128-byte swizzle in this query tile's shared-memory slot
+  // (free: every Q K^T has completed when O is) and one thread of the
+  // group stores the tile with TMA.
+  if (ok) ok = mbar_wait(b_o, 0, abort_flag, P.status);
+  ok = __all_sync(0xffffffffu, ok);
+  tc_fence_after();
+  // the CTA's head and batch, recomputed (not kept live through the loop)
+  const int unit = batched_order(blockIdx.x, P.Hq * P.Bt, nranks, P.unit_batch).unit;
+  const int h = fwd_head(P, unit), bt = fwd_batch(P, unit);
+  if (ok) {
+    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    // all of O's columns in one round trip to tensor memory
+    uint32_t ov[D / 32][32];
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(o_tm + 32 * ch, ov[ch]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      const uint32_t* o = ov[ch];
+      uint32_t wp[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float a = (c > 0) ? __uint_as_float(o[2 * j]) * inv : 0.f;
+        const float b = (c > 0) ? __uint_as_float(o[2 * j + 1]) * inv : 0.f;
+        wp[j] = pack_bf16(a, b);
+      }
+      // columns 32 ch .. 32 ch + 31 = 16-byte chunks 4 ch .. 4 ch + 3 of
+      // the row, in 64-column halves
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c8 = 4 * ch + q, hf = c8 >> 3, chunk = c8 & 7;
+        *reinterpret_cast<uint4*>(stage + hf * kHalfBytes + r * 128 +
+                                  ((chunk ^ (r & 7)) << 4)) =
+            make_uint4(wp[4 * q], wp[4 * q + 1], wp[4 * q + 2], wp[4 * q + 3]);
+      }
+    }
+    fence_proxy_async_smem();  // the staged rows are read next by the TMA unit
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_staged);
+    if (quarter == 0 && lane == 0) {
+      if (mbar_wait(b_staged, 0, abort_flag, P.status)) {
+        const TensorPos t = tensor_pos(P, h, qrow0, bt, P.Hq);
+        for (int hf = 0; hf < kHalves; ++hf)
+          tma_store_4d(tm_o, smem_u32(stage + hf * kHalfBytes), hf * 64, t.h, t.row,
+                       t.b);
+        bulk_commit_group();
+        // the tile has been read out of shared memory before the CTA exits
+        // (the global writes complete on their own)
+        bulk_wait_group_read0();
+      }
+    }
+    P.lse[lse_index(P, bt, h, prow)] =
+        (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+  }
+}
+
 // 10 warps: three share a 16K-register sub-partition, so <= 168 each.
 template <int D>
 __global__ void __maxnreg__(168)
@@ -345,173 +524,14 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int i = warp >> 2;                 // query tile of this group
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;       // row within the tile = TMEM lane
-    const int prow = qbase0 + i * kBM + r;   // permuted query row
-    const RowMask rm = row_mask(P, nat_pos(P, prow));
+    // group i = warp / 4 takes query tile i
+    const int i = warp >> 2, quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + 128 * i;
-    const uint32_t o_tm = tmem + lane_off + 256 + D * i;
-    float m_run = -INFINITY, l_run = 0.f;
-    int c = 0;
-    bool ok = true;
-    while (true) {
-      ok = mbar_wait(bar(L::kInfoFull + i), c & 1, abort_flag, P.status);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      const int2 inf = info[i];
-      if (inf.x == kEnd) break;
-      // a masked tile: this row's visible keys in the tile (the main
-      // interval and the sink interval of row_visible) as one bit per column
-      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
-      if (inf.y == kMasked) {
-        const TileSpan ks = tile_span(P, inf.x * kBN);
-        const ColRange c0 = tile_cols(ks, rm.lo, rm.hi);
-        const ColRange c1 = tile_cols(ks, rm.qs, min(rm.sink_end - 1, rm.causal_hi));
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) vis[ch] = col_bits(c0, 32 * ch) | col_bits(c1, 32 * ch);
-      }
-      ok = mbar_wait(bar(L::kSFull + i), c & 1, abort_flag, P.status);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tm + 32 * ch, sr[ch]);
-      tmem_wait_ld();
-      if (inf.y == kMasked) {
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (!((vis[ch] >> j) & 1u)) sr[ch][j] = __float_as_uint(-INFINITY);
-      }
-      // row max as 8 independent chains (a single chain is latency-bound)
-      float m8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[t >> 5][t & 31]);
-#pragma unroll
-      for (int j = 8; j < 128; ++j)
-        m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      mx *= P.scale_log2;
-      // lazy rescale: move the running max only when it grows by > 2^8
-      const bool need = mx > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx);
-        m_run = mx;
-      }
-      l_run *= alpha;
-      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      // p = exp2(s * scale_log2 - m): scale-and-subtract and the row sum run
-      // on packed fp32 pairs (one FMA-pipe instruction per two elements)
-      const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
-      const uint64_t nm2 = f2_pack(-msub, -msub);
-      uint64_t ls2[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int j0 = 64 * ch + 2 * j;
-          const uint64_t x = f2_fma(
-              f2_pack(__uint_as_float(sr[j0 >> 5][j0 & 31]),
-                      __uint_as_float(sr[(j0 + 1) >> 5][(j0 + 1) & 31])),
-              sc2, nm2);
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ls2[j & 3] = f2_add(ls2[j & 3], f2_pack(p0, p1));
-          pk[j] = pack_bf16(p0, p1);
-        }
-        tmem_st32(s_tm + 32 * ch, pk);
-      }
-      {
-        float a0, a1, b0, b1, c0, c1, d0, d1;
-        f2_unpack(ls2[0], a0, a1);
-        f2_unpack(ls2[1], b0, b1);
-        f2_unpack(ls2[2], c0, c1);
-        f2_unpack(ls2[3], d0, d1);
-        l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-      }
-      // O_i holds PV of the previous tiles (complete: the commit that
-      // signalled S_i tracks every earlier MMA); rescale it to the new max
-      // before P_i V is accumulated onto it.
-      if (__any_sync(0xffffffffu, need && c > 0)) {
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(o_tm + 32 * ch, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st32(o_tm + 32 * ch, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kPFull + i));  // one arrival per warp
-      ++c;
-    }
-    // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2. The rows are
-    // staged in the 128-byte swizzle in this query tile's shared-memory slot
-    // (free: every Q K^T has completed when O is) and one thread of the
-    // group stores the tile with TMA.
-    if (ok) ok = mbar_wait(bar(L::kOFull + i), 0, abort_flag, P.status);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-    // the CTA's head and batch, recomputed (not kept live through the loop)
-    const int unit = fwd_order(P, npairs).unit;
-    const int h = fwd_head(P, unit), bt = fwd_batch(P, unit);
-    if (ok) {
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      uint8_t* stage = sm + L::kQ + i * L::kTileBytes;
-      // all of O's columns in one round trip to tensor memory
-      uint32_t ov[D / 32][32];
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(o_tm + 32 * ch, ov[ch]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        const uint32_t* o = ov[ch];
-        uint32_t wp[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float a = (c > 0) ? __uint_as_float(o[2 * j]) * inv : 0.f;
-          const float b = (c > 0) ? __uint_as_float(o[2 * j + 1]) * inv : 0.f;
-          wp[j] = pack_bf16(a, b);
-        }
-        // columns 32 ch .. 32 ch + 31 = 16-byte chunks 4 ch .. 4 ch + 3 of
-        // the row, in 64-column halves
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c8 = 4 * ch + q, hf = c8 >> 3, chunk = c8 & 7;
-          *reinterpret_cast<uint4*>(stage + hf * L::kHalfBytes + r * 128 +
-                                    ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(wp[4 * q], wp[4 * q + 1], wp[4 * q + 2], wp[4 * q + 3]);
-        }
-      }
-      fence_proxy_async_smem();  // the staged rows are read next by the TMA unit
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kOStaged + i));
-      if (quarter == 0 && lane == 0) {
-        if (mbar_wait(bar(L::kOStaged + i), 0, abort_flag, P.status)) {
-          const TensorPos t = tensor_pos(P, h, qbase0 + i * kBM, bt, P.Hq);
-          for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_store_4d(&tm_o, smem_u32(stage + hf * L::kHalfBytes), hf * 64, t.h, t.row,
-                         t.b);
-          bulk_commit_group();
-          // the tile has been read out of shared memory before the CTA exits
-          // (the global writes complete on their own)
-          bulk_wait_group_read0();
-        }
-      }
-      P.lse[lse_index(P, bt, h, prow)] =
-          (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-    }
+    softmax_tile<D, L::kHalfBytes, L::kHalves>(
+        P, info + i, bar(L::kInfoFull + i), bar(L::kSFull + i), bar(L::kPFull + i),
+        bar(L::kOFull + i), bar(L::kOStaged + i), tmem + lane_off + 128 * i,
+        tmem + lane_off + 256 + D * i, sm + L::kQ + i * L::kTileBytes, &tm_o, qbase0 + i * kBM,
+        quarter, lane, npairs, abort_flag);
   }
 
   tc_fence_before();
@@ -737,156 +757,13 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // One query row per thread, as one group of the two-tile kernel.
+    // one query row per thread, as one group of the two-tile kernel
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const int prow = qbase + r;
-    const RowMask rm = row_mask(P, nat_pos(P, prow));
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off;
-    const uint32_t o_tm = tmem + lane_off + 128;
-    float m_run = -INFINITY, l_run = 0.f;
-    int c = 0;
-    bool ok = true;
-    while (true) {
-      ok = mbar_wait(bar(L::kInfoFull), c & 1, abort_flag, P.status);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      const int2 inf = *info;
-      if (inf.x == kEnd) break;
-      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
-      if (inf.y == kMasked) {
-        const TileSpan ks = tile_span(P, inf.x * kBN);
-        const ColRange c0 = tile_cols(ks, rm.lo, rm.hi);
-        const ColRange c1 = tile_cols(ks, rm.qs, min(rm.sink_end - 1, rm.causal_hi));
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) vis[ch] = col_bits(c0, 32 * ch) | col_bits(c1, 32 * ch);
-      }
-      ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tm + 32 * ch, sr[ch]);
-      tmem_wait_ld();
-      if (inf.y == kMasked) {
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (!((vis[ch] >> j) & 1u)) sr[ch][j] = __float_as_uint(-INFINITY);
-      }
-      float m8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[t >> 5][t & 31]);
-#pragma unroll
-      for (int j = 8; j < 128; ++j)
-        m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      mx *= P.scale_log2;
-      const bool need = mx > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx);
-        m_run = mx;
-      }
-      l_run *= alpha;
-      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
-      const uint64_t nm2 = f2_pack(-msub, -msub);
-      uint64_t ls2[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int j0 = 64 * ch + 2 * j;
-          const uint64_t x = f2_fma(
-              f2_pack(__uint_as_float(sr[j0 >> 5][j0 & 31]),
-                      __uint_as_float(sr[(j0 + 1) >> 5][(j0 + 1) & 31])),
-              sc2, nm2);
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ls2[j & 3] = f2_add(ls2[j & 3], f2_pack(p0, p1));
-          pk[j] = pack_bf16(p0, p1);
-        }
-        tmem_st32(s_tm + 32 * ch, pk);
-      }
-      {
-        float a0, a1, b0, b1, c0, c1, d0, d1;
-        f2_unpack(ls2[0], a0, a1);
-        f2_unpack(ls2[1], b0, b1);
-        f2_unpack(ls2[2], c0, c1);
-        f2_unpack(ls2[3], d0, d1);
-        l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-      }
-      // O holds P V of the previous tiles (complete: the commit that
-      // signalled S tracks every earlier MMA); rescale it to the new max
-      if (__any_sync(0xffffffffu, need && c > 0)) {
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(o_tm + 32 * ch, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st32(o_tm + 32 * ch, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kPFull));  // one arrival per warp
-      ++c;
-    }
-    // epilogue: O / l -> bf16 rows staged in the Q tile (free: every Q K^T
-    // has completed when O is), stored with TMA by one thread
-    if (ok) ok = mbar_wait(bar(L::kOFull), 0, abort_flag, P.status);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-    if (ok) {
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      uint8_t* stage = sm + L::kQ;
-      uint32_t ov[D / 32][32];
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(o_tm + 32 * ch, ov[ch]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        const uint32_t* o = ov[ch];
-        uint32_t wp[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float a = (c > 0) ? __uint_as_float(o[2 * j]) * inv : 0.f;
-          const float b = (c > 0) ? __uint_as_float(o[2 * j + 1]) * inv : 0.f;
-          wp[j] = pack_bf16(a, b);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c8 = 4 * ch + q, hf = c8 >> 3, chunk = c8 & 7;
-          *reinterpret_cast<uint4*>(stage + hf * L::kHalfBytes + r * 128 +
-                                    ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(wp[4 * q], wp[4 * q + 1], wp[4 * q + 2], wp[4 * q + 3]);
-        }
-      }
-      fence_proxy_async_smem();  // the staged rows are read next by the TMA unit
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kOStaged));
-      if (quarter == 0 && lane == 0) {
-        if (mbar_wait(bar(L::kOStaged), 0, abort_flag, P.status)) {
-          const TensorPos t = tensor_pos(P, h, qbase, bt, P.Hq);
-          for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_store_4d(&tm_o, smem_u32(stage + hf * L::kHalfBytes), hf * 64, t.h, t.row,
-                         t.b);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-        }
-      }
-      P.lse[lse_index(P, bt, h, prow)] =
-          (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-    }
+    softmax_tile<D, L::kHalfBytes, L::kHalves>(
+        P, info, bar(L::kInfoFull), bar(L::kSFull), bar(L::kPFull), bar(L::kOFull),
+        bar(L::kOStaged), tmem + lane_off, tmem + lane_off + 128, sm + L::kQ, &tm_o, qbase,
+        quarter, lane, ntiles, abort_flag);
   }
 
   tc_fence_before();
