@@ -20,6 +20,7 @@ CASES = [
     (2, 2, 256, 2, 1, 64, 1, 1, True, False),
     (1, 16, 4096, 1, 1, 128, 8, 8, True, True),  # 64 partials, 16 rows per KV head
     (1, 16, 128, 1, 1, 64, 1, 2, True, True),    # the last piece partly masked
+    (2, 2, 1024, 8, 2, 128, 2, 2, True, True),   # 8 rows per KV head (five stages)
 ]
 
 
