@@ -161,6 +161,7 @@ typedef enum {
  *      B is then the number of sequences and the layout applies to the
  *      packed sequence. The values are trusted (not checked on the device):
  *      malformed boundaries give wrong masks but no out-of-bounds access.
+ *      usp_check_cu_seqlens checks a host copy (the debug-mode check).
  * cp_size >= 1, ulysses_degree >= 1, layout, dtype (q/k/v/out element type).
  * flags  USP_FLAG_*.
  * workspace / workspace_bytes  caller scratch of at least
@@ -183,6 +184,22 @@ usp_status_t usp_attn_fwd(const void *q, const void *k, const void *v,
 size_t usp_attn_fwd_workspace_size(int B, int S, int Hq, int Hkv, int D,
                                    int cp_size, int ulysses_degree,
                                    usp_dtype_t dtype, unsigned flags);
+
+/*
+ * usp_check_cu_seqlens - the debug-mode check of packed-sequence boundaries.
+ *
+ * The attention calls trust their cu_seqlens (a device array: checking it
+ * would need a synchronisation). A caller that wants it checked copies it to
+ * the host and passes the copy here (the boundaries of the packed batch, as
+ * the ring-sliding-window README's "Arguments" define cu_seqlens: global over
+ * all ranks): cu_seqlens_host [nseq + 1] int32, HOST
+ * memory, read only. Returns USP_OK when cu_seqlens_host[0] == 0, the
+ * values never decrease and cu_seqlens_host[nseq] == total_tokens (the S of
+ * the attention call); else USP_ERR_INVALID_ARG, with the first offending
+ * index in usp_last_error_detail(). nseq >= 1 and a non-NULL pointer are
+ * required (USP_ERR_INVALID_ARG otherwise). Touches no device state.
+ */
+usp_status_t usp_check_cu_seqlens(const int32_t *cu_seqlens_host, int nseq, int total_tokens);
 
 /*
  * usp_attn_bwd - gradients of usp_attn_fwd from the saved (out, lse).
@@ -485,7 +502,8 @@ usp_status_t usp_device_status(void);
 usp_status_t usp_selftest_wait_timeout(unsigned limit_us, usp_stream_t stream);
 
 /* Which CUDA call failed, and why, for the last USP_ERR_CUDA returned on the
- * calling thread (thread-local storage, never NULL; empty if none). */
+ * calling thread, or why an argument was refused where a call's description
+ * says so (thread-local storage, never NULL; empty if none). */
 const char *usp_last_error_detail(void);
 
 /* Human-readable name of a status code (static storage, never NULL). */

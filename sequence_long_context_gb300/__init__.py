@@ -162,6 +162,16 @@ def usp_permute(src, dst, kind, layout, B, S, H, D, cp_size, ulysses_degree,
         D, cp_size, ulysses_degree, elem_bytes, _stream(stream)))
 
 
+def usp_check_cu_seqlens(cu_seqlens_host, nseq, total_tokens) -> None:
+    """Raise unless cu_seqlens_host (int32, host) starts at 0, never
+    decreases and ends at total_tokens (the debug-mode check)."""
+    st = _lib.load().usp_check_cu_seqlens(_p(cu_seqlens_host), int(nseq), int(total_tokens))
+    if st != 0:
+        lib = _lib.load()
+        raise UspError(lib.usp_status_string(st).decode() + ": "
+                       + lib.usp_last_error_detail().decode())
+
+
 def usp_launch_count() -> int:
     return int(_lib.load().usp_launch_count())
 
@@ -207,6 +217,15 @@ def _packed_dims(qkv: torch.Tensor, cu_seqlens):
         return int(cu_seqlens.numel() - 1), T, H, D, 1
     B, S, _, H, D = qkv.shape
     return B, S, H, D, B
+
+
+def check_cu_seqlens(cu_seqlens: torch.Tensor, total_tokens: int) -> None:
+    """Check packed-sequence boundaries on the host before a call (the
+    attention calls trust them); copies a device tensor to the host."""
+    cu = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+    if cu.dim() != 1 or cu.numel() < 2:
+        raise UspError("USP_ERR_INVALID_ARG: cu_seqlens needs at least two entries")
+    usp_check_cu_seqlens(cu, cu.numel() - 1, total_tokens)
 
 
 def attn_forward_qkvpacked(qkv, *, causal=True, window=0, sink_tokens=0,

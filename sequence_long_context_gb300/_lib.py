@@ -42,6 +42,7 @@ SIGNATURES = {
     "usp_profile_read": (_i, [_vp, _i]),
     "usp_device_status": (_i, []),
     "usp_last_error_detail": (_c.c_char_p, []),
+    "usp_check_cu_seqlens": (_i, [_vp, _i, _i]),
 }
 
 

@@ -292,6 +292,30 @@ using namespace usp;
 
 extern "C" {
 
+usp_status_t usp_check_cu_seqlens(const int32_t* cu, int nseq, int total) {
+  if (cu == nullptr || nseq < 1 || total < 0) return USP_ERR_INVALID_ARG;
+  char msg[96];
+  if (cu[0] != 0) {
+    std::snprintf(msg, sizeof(msg), "cu_seqlens[0] = %d, not 0", (int)cu[0]);
+    set_error_detail(msg);
+    return USP_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < nseq; ++i)
+    if (cu[i + 1] < cu[i]) {
+      std::snprintf(msg, sizeof(msg), "cu_seqlens[%d] = %d < cu_seqlens[%d] = %d", i + 1,
+                    (int)cu[i + 1], i, (int)cu[i]);
+      set_error_detail(msg);
+      return USP_ERR_INVALID_ARG;
+    }
+  if (cu[nseq] != total) {
+    std::snprintf(msg, sizeof(msg), "cu_seqlens[%d] = %d, not the %d tokens", nseq,
+                  (int)cu[nseq], total);
+    set_error_detail(msg);
+    return USP_ERR_INVALID_ARG;
+  }
+  return USP_OK;
+}
+
 const char* usp_status_string(usp_status_t st) {
   switch (st) {
     case USP_OK: return "USP_OK";

@@ -287,3 +287,35 @@ def test_natural_order_flag_host_checks(lib):
     assert lib.usp_attn_bwd_qkvpacked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 64, 0.0, 1, 0,
                                       0, None, 4, 1, 1, 1, N, None, 0, None) == 2
     assert fp8_fwd(lib, flags=N) == 2
+
+
+@pytest.mark.parametrize("cu,total,ok,detail", [
+    ([0, 128], 128, True, None),
+    ([0, 100, 100, 512], 512, True, None),   # an empty sequence is allowed
+    ([0, 0], 0, True, None),
+    ([1, 128], 128, False, b"cu_seqlens[0]"),
+    ([0, 300, 200, 512], 512, False, b"cu_seqlens[2] = 200"),
+    ([0, 100, 500], 512, False, b"not the 512 tokens"),
+    ([0, 100, 600], 512, False, b"not the 512 tokens"),
+])
+def test_check_cu_seqlens(lib, cu, total, ok, detail):
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    st = lib.usp_check_cu_seqlens(ctypes.addressof(arr), len(cu) - 1, total)
+    assert st == (0 if ok else 1)
+    if detail is not None:
+        assert detail in lib.usp_last_error_detail()
+    t = torch.tensor(cu, dtype=torch.int32)
+    if ok:
+        usp.check_cu_seqlens(t, total)
+    else:
+        with pytest.raises(usp.UspError, match="INVALID_ARG"):
+            usp.check_cu_seqlens(t, total)
+
+
+def test_check_cu_seqlens_rejects_bad_arguments(lib):
+    arr = (ctypes.c_int32 * 2)(0, 8)
+    assert lib.usp_check_cu_seqlens(None, 1, 8) == 1
+    assert lib.usp_check_cu_seqlens(ctypes.addressof(arr), 0, 8) == 1
+    assert lib.usp_check_cu_seqlens(ctypes.addressof(arr), 1, -1) == 1
+    with pytest.raises(usp.UspError):
+        usp.check_cu_seqlens(torch.tensor([0], dtype=torch.int32), 0)
