@@ -12,25 +12,28 @@
 // written once (the shard's ring return). dQ contributions are added into an
 // fp32 accumulator in global memory by TMA reduce-add operations.
 //
-// Roles (704 threads):
+// Roles (608 threads):
 //   warps 0-15  softmax, four threads per key row (warp w owns query columns
 //              [32 (w/4), 32 (w/4) + 32)): P^T = exp2(S^T - LSE),
 //              dS^T = P^T (dP^T - Delta); P^T and dS^T go back to tensor
 //              memory as bf16 (A operands of dV and dK) and dS to shared
 //              memory (A operand of dQ). No row reductions are needed (P
 //              comes from the saved LSE), so the columns split freely; four
-//              warps per TMEM lane quarter hide the latency of each phase
-//   warps 16-19 dQ group, one query row per thread: takes the dQ tile out of
-//              tensor memory (freeing it for the next tile's dP^T), stages
-//              it in the dS tile and the dO half of the tile's ring slot
-//              (both dead once the tile's dQ MMA is done), and has the TMA
-//              unit add it into the global fp32 accumulator; the dS tile
-//              and the dO half go back once the TMA has read them
-//   warp 20    producer: K, V once; then Q, dO tiles through a 2-slot ring.
+//              warps per TMEM lane quarter hide the latency of each phase.
+//              Then, while the next tile's S^T is computed, the same warps
+//              take the tile's dQ out of tensor memory (warp w: query rows
+//              [32 (w%4), +32), dQ columns [32 (w/4), +32); one load each,
+//              freeing the columns for the next dP^T) and stage it, scaled,
+//              in the dS tile and the dO half of the tile's ring slot (both
+//              dead once the tile's dQ MMA is done)
+//   warp 16    dQ reduction: has the TMA unit add the staged dQ into the
+//              global fp32 accumulator, and hands the dS tile and the dO
+//              half back once the TMA has read them
+//   warp 17    producer: K, V once; then Q, dO tiles through a 2-slot ring.
 //              The Q half of a slot (Q tile, LSE and Delta rows) is refilled
 //              as soon as the tile's last MMA (dK, which reads Q) is done;
-//              the dO half once the dQ drain hands it back
-//   warp 21    MMA issuer and tensor-memory owner
+//              the dO half once the dQ reduction hands it back
+//   warp 18    MMA issuer and tensor-memory owner
 // Tensor memory (512 columns): S^T [0,128); the 32 queries of column chunk
 // c live in columns [32c, 32c+32) and are overwritten in place by their P^T
 // (bf16 pairs, first 16 columns) and dS^T (last 16); dP^T [128,256),
@@ -51,10 +54,10 @@ using namespace tc;
 __device__ int g_bwd_tc_status = 0;
 
 constexpr int kSoftWarps = 16;  // four per TMEM lane quarter, one per 32 queries
-constexpr int kDrainWarp0 = kSoftWarps;
-constexpr int kProducerWarp = kDrainWarp0 + 4;
+constexpr int kReduceWarp = kSoftWarps;
+constexpr int kProducerWarp = kReduceWarp + 1;
 constexpr int kMmaWarp = kProducerWarp + 1;
-constexpr int kThreads = 32 * (kMmaWarp + 1);  // 704
+constexpr int kThreads = 32 * (kMmaWarp + 1);  // 608
 constexpr int kEnd = -1;
 
 template <int D>
@@ -74,14 +77,16 @@ struct BSmem {
   static constexpr int kBar = kStats + 2 * kStatBytes;
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
-                       kDKVFull = 12, kMmaDone = 13, kPReady = 14, kDQGroup = 15,
+                       kDKVFull = 12, kMmaDone = 13, kPReady = 14, kDQStaged = 15,
                        kDSFree = 16, kDOFull = 17, kStageFreeDO = 19, kKVStaged = 21,
                        kNumBars = 23;
   // Each Q/dO slot has two halves with their own full/free barriers: the Q
   // half (Q tile, LSE and Delta rows; kQFull / kQEmpty, the commit of the
   // tile's last MMA) and the dO half (kDOFull / kStageFreeDO, handed back by
-  // the dQ drain, which stages through it). kDSFree: the dS tile may take
-  // the next tile's dS (the drain's staging in it has been read).
+  // the dQ reduction; dQ is staged through it). kDSFree: the dS tile may take
+  // the next tile's dS (the dQ staged in it has been read by the TMA unit).
+  // kDQEmpty: the dQ columns have been read (and the reduction warp has read
+  // the tile's entry); kDQStaged: every dQ row is staged.
   // 16-byte aligned: int4 / float4 accesses below
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
@@ -118,10 +123,10 @@ __device__ __forceinline__ ColMask col_mask(const AttnParams& P, int j) {
   return m;
 }
 
-// 22 warps: six share a 16K-register sub-partition, so <= 85 each (80 in
+// 19 warps: five share a 16K-register sub-partition, so <= 102 each (96 in
 // the allocation's steps of 8).
 template <int D>
-__global__ void __maxnreg__(80)
+__global__ void __maxnreg__(96)
 attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
@@ -130,6 +135,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_dk,
                    const __grid_constant__ CUtensorMap tm_dv) {
   using L = BSmem<D>;
+  // dQ staging: D/32 boxes of 32 fp32 columns x 128 rows (16 KB each) in the
+  // 128-byte swizzle; the first two fill the dS tile (32 KB), the rest the dO
+  // half of the tile's slot. The softmax warps of column chunks ch < D/32
+  // read and stage box ch.
+  constexpr int kBoxBytes = kTile * 128;
+  constexpr int kBoxes = D / 32;
+  constexpr int kBoxesInDS = kBoxes < 2 ? kBoxes : 2;
+  constexpr int kDQWarps = 4 * kBoxes;
+  static_assert(kBoxesInDS * kBoxBytes <= kTile * kTile * 2, "staging exceeds the dS tile");
+  static_assert((kBoxes - kBoxesInDS) * kBoxBytes <= L::kTileBytes,
+                "staging exceeds the dO half");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled tiles need a 1024-byte aligned window; there is no slack to
   // realign into, so a misaligned window is reported and the CTA does nothing
@@ -140,6 +156,10 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   uint8_t* sm = smem_raw;
   const uint32_t sbase = smem_u32(sm);
   auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
+  auto stage_box = [&](int slot, int cg) -> uint8_t* {
+    return cg < kBoxesInDS ? sm + L::kDS + cg * kBoxBytes
+                           : sm + L::kDO + slot * L::kTileBytes + (cg - kBoxesInDS) * kBoxBytes;
+  };
   int4* sched = reinterpret_cast<int4*>(sm + L::kSched);
   int4* info = reinterpret_cast<int4*>(sm + L::kInfo);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kMisc);
@@ -164,9 +184,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kDPFull), 1);
     mbar_init(bar(L::kDSFull), kSoftWarps);  // one arrival per softmax warp
     mbar_init(bar(L::kDQFull), 1);
-    mbar_init(bar(L::kDQEmpty), kTile / 32);  // one arrival per drain warp
-    mbar_init(bar(L::kDQGroup), kTile);
-    for (int s = 0; s < 2; ++s) {  // dO halves, handed back by the dQ drain
+    // one arrival per softmax warp that reads dQ columns, and one by the
+    // reduction warp once it has read the tile's entry
+    mbar_init(bar(L::kDQEmpty), kDQWarps + 1);
+    mbar_init(bar(L::kDQStaged), kDQWarps);   // one arrival per such warp
+    for (int s = 0; s < 2; ++s) {  // dO halves, handed back by the dQ reduction
       mbar_init(bar(L::kStageFreeDO + s), 1);
       mbar_init(bar(L::kDOFull + s), 1);
     }
@@ -230,7 +252,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
             const int h = g * P.G + hh;
             const int slot = n & 1, use = n >> 1;
             // the Q half is free once the MMAs of its previous tile are done;
-            // the dO half once the dQ drain has used it as staging
+            // the dO half once the dQ reduction has used it as staging
             if (use >= 1 && !(ok = mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1,
                                              abort_flag, P.status)))
               break;
@@ -287,7 +309,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     // S^T columns, 16 queries per MMA), overlapping the softmax's dS; when dS
     // is ready: dQ = dS K into [128,256) as one N=D block, then
     // dK += dS^T Q. The next S^T only has to follow this tile's dV/dK in
-    // issue order, never the dQ drain.
+    // issue order, never the dQ reduction.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, 0, 0);
       constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, D, 1, 1);
@@ -323,8 +345,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kSFull));
-        // the previous dQ must have left [128,256) (and the drain must have
-        // read its entry) before dP^T and the next drain entry
+        // the previous dQ must have left [128,256) (and the reduction warp
+        // must have read its entry) before dP^T and the next entry
         if (n > 0 && !(ok = mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status)))
           break;
         if (!(ok = mbar_wait(bar(L::kDOFull + slot), use & 1, abort_flag, P.status))) break;
@@ -366,7 +388,7 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       mma_commit(bar(L::kDKVFull));
       info[0] = make_int4(kEnd, n, 0, 0);
       mbar_arrive(bar(L::kInfoS));
-      // the dQ group must have consumed the last real entry before the
+      // the reduction warp must have read the last real entry before the
       // end marker overwrites it
       if (ok && n > 0) mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status);
       info[1] = make_int4(kEnd, n, 0, 0);
@@ -478,6 +500,38 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kDSFull));
+      if (ch < kBoxes) {
+        // this tile's dQ, rows [32 quarter, +32) x columns [32 ch, +32): out
+        // of tensor memory as soon as the dQ MMA is done (the columns go back
+        // for the next dP^T), then staged, scaled, for the reduction warp.
+        // The next S^T is being computed meanwhile. Once the dQ MMA is done,
+        // nothing reads the dS tile or the dO half of the tile's slot any
+        // more (the dP^T and dV MMAs that read dO were issued before it), and
+        // neither is written again before the reduction hands it back.
+        ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(t_dp, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kDQEmpty));
+        const int i = quarter * 32 + lane;  // query row = TMEM lane
+        uint8_t* rowp = stage_box(c & 1, ch) + i * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 x = make_float4(__uint_as_float(v[4 * k]) * P.scale,
+                                       __uint_as_float(v[4 * k + 1]) * P.scale,
+                                       __uint_as_float(v[4 * k + 2]) * P.scale,
+                                       __uint_as_float(v[4 * k + 3]) * P.scale);
+          *reinterpret_cast<float4*>(rowp + ((k ^ (i & 7)) << 4)) = x;
+        }
+        // read next by the TMA unit (async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kDQStaged));
+      }
       ++c;
     }
     // epilogue: warps 0-3 write dV, warps 4-7 scale * dK for their key
@@ -526,77 +580,28 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         bulk_wait_group_read0();
       }
     }
-  } else {
-    // ------------------------------------------------------------ dQ drain
-    const int qw = warp - kDrainWarp0;
-    const int i = qw * 32 + lane;  // query row = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+  } else if (warp == kReduceWarp) {
+    // ------------------------------------------------------------ dQ reduction
+    // Per query tile: the staged dQ boxes are added into the global fp32
+    // accumulator by the TMA unit. The dS tile's boxes go first, as their own
+    // bulk group: the softmax waits for that space before it writes the next
+    // tile's dS. Each space goes back as soon as the TMA has read it; the
+    // additions complete asynchronously. The Q half of the slot is not used,
+    // so the producer can refill it as soon as the tile's dK MMA is done.
     int c = 0;
-    // bounded barrier of the 128 drain threads (parity of the use count)
-    auto group_sync = [&](int b, int use) -> bool {
-      mbar_arrive(bar(b));
-      return __all_sync(0xffffffffu, mbar_wait(bar(b), use & 1, abort_flag, P.status));
-    };
-    // staging box cg (32 fp32 columns x 128 rows, 16 KB): the first two fill
-    // the dS tile (32 KB), the rest the dO half of the tile's slot
-    constexpr int kBoxBytes = kTile * 128;
-    constexpr int kBoxes = D / 32;
-    constexpr int kBoxesInDS = kBoxes < 2 ? kBoxes : 2;
-    static_assert(kBoxesInDS * kBoxBytes <= kTile * kTile * 2, "staging exceeds the dS tile");
-    static_assert((kBoxes - kBoxesInDS) * kBoxBytes <= L::kTileBytes,
-                  "staging exceeds the dO half");
-    auto stage_box = [&](int slot, int cg) -> uint8_t* {
-      return cg < kBoxesInDS ? sm + L::kDS + cg * kBoxBytes
-                             : sm + L::kDO + slot * L::kTileBytes + (cg - kBoxesInDS) * kBoxBytes;
-    };
-    const bool leader = qw == 0 && lane == 0;  // issues the reductions
-    auto release_tmem = [&]() {  // every dQ column has been read
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kDQEmpty));
-    };
     while (true) {
       bool ok = mbar_wait(bar(L::kInfoQ), c & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int4 e = info[1];
       if (e.x == kEnd) break;
       const int qt = e.x, h = e.y;
-      ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
+      // the entry has been read: the MMA warp may post the next one
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kDQEmpty));
+      ok = mbar_wait(bar(L::kDQStaged), c & 1, abort_flag, P.status);
       if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      // Once this tile's dQ MMA is done, nothing reads its dS tile or the dO
-      // half of its slot any more (the dP^T and dV MMAs that read dO were
-      // issued before it), and neither is written again before this drain
-      // hands it back: dQ is staged there, scaled, as D/32 boxes of 32 fp32
-      // columns x 128 rows in the 128-byte swizzle (16-byte chunk k of row r
-      // at k ^ (r & 7)), and one thread hands the boxes to the TMA unit,
-      // which adds them into the global fp32 accumulator. Each space goes
-      // back as soon as the TMA has read it; the additions complete
-      // asynchronously. The Q half of the slot is not used, so the producer
-      // can refill it as soon as the tile's dK MMA is done.
       const int slot = c & 1;
-#pragma unroll
-      for (int cg = 0; cg < kBoxes; ++cg) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + 128 + 32 * cg, v);
-        tmem_wait_ld();
-        if (cg + 1 == kBoxes) release_tmem();
-        uint8_t* rowp = stage_box(slot, cg) + i * 128;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 x = make_float4(__uint_as_float(v[4 * k]) * P.scale,
-                                       __uint_as_float(v[4 * k + 1]) * P.scale,
-                                       __uint_as_float(v[4 * k + 2]) * P.scale,
-                                       __uint_as_float(v[4 * k + 3]) * P.scale);
-          *reinterpret_cast<float4*>(rowp + ((k ^ (i & 7)) << 4)) = x;
-        }
-      }
-      // the staged rows are read next by the TMA unit (async proxy)
-      fence_proxy_async_smem();
-      if (!(ok = group_sync(L::kDQGroup, c))) break;  // all rows staged
-      if (leader) {
-        // the dS tile's boxes first, as their own bulk group: the softmax
-        // waits for that space before it writes the next tile's dS
+      if (lane == 0) {
 #pragma unroll
         for (int cg = 0; cg < kBoxes; ++cg) {
           tma_reduce_add_4d(&tm_dq, smem_u32(stage_box(slot, cg)), 32 * cg, h, qt * kTile, bt);
@@ -613,10 +618,11 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         }
         mbar_arrive(bar(L::kStageFreeDO + slot));
       }
+      __syncwarp();
       ++c;
     }
     // every reduction has landed before the CTA exits
-    if (leader) bulk_wait_group0();
+    if (lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
