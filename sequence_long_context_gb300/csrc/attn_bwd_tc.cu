@@ -433,15 +433,18 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (ok) ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
+      // P^T = exp2(S^T scale log2e - LSE log2e): kept in fp32 registers for
+      // dS, and written over the S^T columns as bf16 pairs for dV
+      float pf[32];
       {
-        // P^T = exp2(S^T scale log2e - LSE log2e) -> bf16 pairs
         uint32_t sv[32];
         tmem_ld32(t_s, sv);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float2 l = reinterpret_cast<const float2*>(lse2)[k];
+          const float4 l4 = reinterpret_cast<const float4*>(lse2)[k >> 1];
+          const float2 l = (k & 1) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
                                     sc2, f2_pack(-l.x, -l.y));
           float x0, x1;
@@ -453,6 +456,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
             if (i0 < cm.lo || i0 > cm.hi) p0 = 0.f;
             if (i1 < cm.lo || i1 > cm.hi) p1 = 0.f;
           }
+          pf[2 * k] = p0;
+          pf[2 * k + 1] = p1;
           pk[k] = pack_bf16(p0, p1);
         }
         tmem_st16(t_s, pk);  // own columns, already read
@@ -469,20 +474,17 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       {
-        // dS^T = P^T (dP^T - Delta)
+        // dS^T = P^T (dP^T - Delta) on packed pairs, P from the P phase
         uint32_t dv[32], pv[16];
         tmem_ld32(t_dp, dv);
-        tmem_ld16(t_s, pv);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float2 dl = reinterpret_cast<const float2*>(delta)[k];
-          __nv_bfloat162 pp = *reinterpret_cast<__nv_bfloat162*>(&pv[k]);
-          const float2 pf = __bfloat1622float2(pp);
-          // dS = P dP - P Delta on packed pairs
-          const uint64_t p2 = f2_pack(pf.x, pf.y);
-          const uint64_t ds2 = f2_fma(p2, f2_pack(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1])),
-                                      f2_pack(-pf.x * dl.x, -pf.y * dl.y));
+          const float4 d4 = reinterpret_cast<const float4*>(delta)[k >> 1];
+          const float2 dl = (k & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+          const uint64_t d2 = f2_add(f2_pack(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1])),
+                                     f2_pack(-dl.x, -dl.y));
+          const uint64_t ds2 = f2_mul(f2_pack(pf[2 * k], pf[2 * k + 1]), d2);
           float d0, d1;
           f2_unpack(ds2, d0, d1);
           pv[k] = pack_bf16(d0, d1);
