@@ -24,15 +24,14 @@
 //              take the tile's dQ out of tensor memory (warp w: query rows
 //              [32 (w%4), +32), dQ columns [32 (w/4), +32); one load each,
 //              freeing the columns for the next dP^T) and stage it, scaled,
-//              in the dS tile and the dO half of the tile's ring slot (both
-//              dead once the tile's dQ MMA is done)
+//              in the Q and dO tiles of the tile's ring slot (dead once the
+//              tile's dK and dQ MMAs are done)
 //   warp 16    dQ reduction: has the TMA unit add the staged dQ into the
-//              global fp32 accumulator, and hands the dS tile and the dO
-//              half back once the TMA has read them
-//   warp 17    producer: K, V once; then Q, dO tiles through a 2-slot ring.
-//              The Q half of a slot (Q tile, LSE and Delta rows) is refilled
-//              as soon as the tile's last MMA (dK, which reads Q) is done;
-//              the dO half once the dQ reduction hands it back
+//              global fp32 accumulator, and hands the Q and dO halves of the
+//              slot back once the TMA has read them
+//   warp 17    producer: K, V once; then Q, dO tiles through a 2-slot ring;
+//              each half of a slot (the Q half also holds the LSE and Delta
+//              rows) is refilled once the dQ reduction hands it back
 //   warp 18    MMA issuer and tensor-memory owner
 // Tensor memory (512 columns): S^T [0,128); the 32 queries of column chunk
 // c live in columns [32c, 32c+32) and are overwritten in place by their P^T
@@ -78,15 +77,16 @@ struct BSmem {
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kDPFull = 6,
                        kDSFull = 7, kDQFull = 8, kDQEmpty = 9, kInfoS = 10, kInfoQ = 11,
                        kDKVFull = 12, kMmaDone = 13, kPReady = 14, kDQStaged = 15,
-                       kDSFree = 16, kDOFull = 17, kStageFreeDO = 19, kKVStaged = 21,
-                       kNumBars = 23;
+                       kDOFull = 16, kStageFreeDO = 18, kStageFreeQ = 20, kKVStaged = 22,
+                       kNumBars = 24;
   // Each Q/dO slot has two halves with their own full/free barriers: the Q
-  // half (Q tile, LSE and Delta rows; kQFull / kQEmpty, the commit of the
-  // tile's last MMA) and the dO half (kDOFull / kStageFreeDO, handed back by
-  // the dQ reduction; dQ is staged through it). kDSFree: the dS tile may take
-  // the next tile's dS (the dQ staged in it has been read by the TMA unit).
-  // kDQEmpty: the dQ columns have been read (and the reduction warp has read
-  // the tile's entry); kDQStaged: every dQ row is staged.
+  // half (Q tile, LSE and Delta rows; kQFull / kStageFreeQ) and the dO half
+  // (kDOFull / kStageFreeDO). Once the tile's dQ MMA is done (the dO half)
+  // and its dK MMA too (kQEmpty, the commit of the tile's last MMA: the Q
+  // tile), the tile's dQ is staged through both, and the dQ reduction hands
+  // each back when the TMA unit has read it. kDQEmpty: the dQ columns have
+  // been read (and the reduction warp has read the tile's entry);
+  // kDQStaged: every dQ row is staged.
   // 16-byte aligned: int4 / float4 accesses below
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
   static constexpr int kInfo = kSched + 32;           // int4 x 2 (softmax, dQ)
@@ -136,15 +136,15 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_dv) {
   using L = BSmem<D>;
   // dQ staging: D/32 boxes of 32 fp32 columns x 128 rows (16 KB each) in the
-  // 128-byte swizzle; the first two fill the dS tile (32 KB), the rest the dO
-  // half of the tile's slot. The softmax warps of column chunks ch < D/32
-  // read and stage box ch.
+  // 128-byte swizzle; the first half fill the Q tile of the tile's slot, the
+  // rest its dO tile. The softmax warps of column chunks ch < D/32 read and
+  // stage box ch.
   constexpr int kBoxBytes = kTile * 128;
   constexpr int kBoxes = D / 32;
-  constexpr int kBoxesInDS = kBoxes < 2 ? kBoxes : 2;
+  constexpr int kBoxesInQ = L::kTileBytes / kBoxBytes;
   constexpr int kDQWarps = 4 * kBoxes;
-  static_assert(kBoxesInDS * kBoxBytes <= kTile * kTile * 2, "staging exceeds the dS tile");
-  static_assert((kBoxes - kBoxesInDS) * kBoxBytes <= L::kTileBytes,
+  static_assert(kBoxesInQ >= 1 && kBoxesInQ < kBoxes, "staging needs both halves");
+  static_assert((kBoxes - kBoxesInQ) * kBoxBytes <= L::kTileBytes,
                 "staging exceeds the dO half");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled tiles need a 1024-byte aligned window; there is no slack to
@@ -157,8 +157,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   const uint32_t sbase = smem_u32(sm);
   auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
   auto stage_box = [&](int slot, int cg) -> uint8_t* {
-    return cg < kBoxesInDS ? sm + L::kDS + cg * kBoxBytes
-                           : sm + L::kDO + slot * L::kTileBytes + (cg - kBoxesInDS) * kBoxBytes;
+    return cg < kBoxesInQ ? sm + L::kQ + slot * L::kTileBytes + cg * kBoxBytes
+                          : sm + L::kDO + slot * L::kTileBytes + (cg - kBoxesInQ) * kBoxBytes;
   };
   int4* sched = reinterpret_cast<int4*>(sm + L::kSched);
   int4* info = reinterpret_cast<int4*>(sm + L::kInfo);
@@ -190,9 +190,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kDQStaged), kDQWarps);   // one arrival per such warp
     for (int s = 0; s < 2; ++s) {  // dO halves, handed back by the dQ reduction
       mbar_init(bar(L::kStageFreeDO + s), 1);
+      mbar_init(bar(L::kStageFreeQ + s), 1);
       mbar_init(bar(L::kDOFull + s), 1);
     }
-    mbar_init(bar(L::kDSFree), 1);
     mbar_init(bar(L::kInfoS), 1);
     mbar_init(bar(L::kInfoQ), 1);
     mbar_init(bar(L::kDKVFull), 1);
@@ -251,9 +251,8 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
           for (int hh = 0; hh < P.G && ok; ++hh) {
             const int h = g * P.G + hh;
             const int slot = n & 1, use = n >> 1;
-            // the Q half is free once the MMAs of its previous tile are done;
-            // the dO half once the dQ reduction has used it as staging
-            if (use >= 1 && !(ok = mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1,
+            // each half is free once the dQ reduction has used it as staging
+            if (use >= 1 && !(ok = mbar_wait(bar(L::kStageFreeQ + slot), (use - 1) & 1,
                                              abort_flag, P.status)))
               break;
             sched[slot] = make_int4(qt, h, cls, 0);
@@ -282,13 +281,13 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       }
       if (ok) {
         const int slot = n & 1, use = n >> 1;
-        if (use < 1 || mbar_wait(bar(L::kQEmpty + slot), (use - 1) & 1, abort_flag,
+        if (use < 1 || mbar_wait(bar(L::kStageFreeQ + slot), (use - 1) & 1, abort_flag,
                                  P.status)) {
           sched[slot] = make_int4(kEnd, 0, 0, 0);
           mbar_arrive(bar(L::kQFull + slot));
         }
         for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
-          if (!mbar_wait(bar(L::kQEmpty + (m & 1)), (m >> 1) & 1, abort_flag, P.status) ||
+          if (!mbar_wait(bar(L::kStageFreeQ + (m & 1)), (m >> 1) & 1, abort_flag, P.status) ||
               !mbar_wait(bar(L::kStageFreeDO + (m & 1)), (m >> 1) & 1, abort_flag, P.status))
             break;
       }
@@ -467,10 +466,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kPReady));
+      // (the dS tile is free: the previous tile's dQ MMA, its only reader,
+      // completed before this tile's S^T)
       ok = mbar_wait(bar(L::kDPFull), c & 1, abort_flag, P.status);
-      // the dS tile holds the previous tile's dQ staging until the TMA has
-      // read it (and before that its dS, read by that tile's dQ MMA)
-      if (ok && c > 0) ok = mbar_wait(bar(L::kDSFree), (c - 1) & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       {
@@ -507,9 +505,10 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         // of tensor memory as soon as the dQ MMA is done (the columns go back
         // for the next dP^T), then staged, scaled, for the reduction warp.
         // The next S^T is being computed meanwhile. Once the dQ MMA is done,
-        // nothing reads the dS tile or the dO half of the tile's slot any
-        // more (the dP^T and dV MMAs that read dO were issued before it), and
-        // neither is written again before the reduction hands it back.
+        // nothing reads the dO tile of the tile's slot any more (the dP^T and
+        // dV MMAs that read it were issued before), and once the dK MMA is
+        // done nothing reads its Q tile; neither is written again before the
+        // reduction hands it back.
         ok = mbar_wait(bar(L::kDQFull), c & 1, abort_flag, P.status);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
@@ -519,6 +518,10 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::kDQEmpty));
+        if (ch < kBoxesInQ) {
+          ok = mbar_wait(bar(L::kQEmpty + (c & 1)), (c >> 1) & 1, abort_flag, P.status);
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        }
         const int i = quarter * 32 + lane;  // query row = TMEM lane
         uint8_t* rowp = stage_box(c & 1, ch) + i * 128;
 #pragma unroll
@@ -585,11 +588,9 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
   } else if (warp == kReduceWarp) {
     // ------------------------------------------------------------ dQ reduction
     // Per query tile: the staged dQ boxes are added into the global fp32
-    // accumulator by the TMA unit. The dS tile's boxes go first, as their own
-    // bulk group: the softmax waits for that space before it writes the next
-    // tile's dS. Each space goes back as soon as the TMA has read it; the
-    // additions complete asynchronously. The Q half of the slot is not used,
-    // so the producer can refill it as soon as the tile's dK MMA is done.
+    // accumulator by the TMA unit, the Q tile's boxes first as their own bulk
+    // group. Each space goes back to the producer as soon as the TMA has read
+    // it; the additions complete asynchronously.
     int c = 0;
     while (true) {
       bool ok = mbar_wait(bar(L::kInfoQ), c & 1, abort_flag, P.status);
@@ -607,17 +608,12 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int cg = 0; cg < kBoxes; ++cg) {
           tma_reduce_add_4d(&tm_dq, smem_u32(stage_box(slot, cg)), 32 * cg, h, qt * kTile, bt);
-          if (cg + 1 == kBoxesInDS && kBoxesInDS < kBoxes) bulk_commit_group();
+          if (cg + 1 == kBoxesInQ) bulk_commit_group();
         }
         bulk_commit_group();
-        if constexpr (kBoxesInDS < kBoxes) {
-          bulk_wait_group_read1();
-          mbar_arrive(bar(L::kDSFree));
-          bulk_wait_group_read0();
-        } else {
-          bulk_wait_group_read0();
-          mbar_arrive(bar(L::kDSFree));
-        }
+        bulk_wait_group_read1();
+        mbar_arrive(bar(L::kStageFreeQ + slot));
+        bulk_wait_group_read0();
         mbar_arrive(bar(L::kStageFreeDO + slot));
       }
       __syncwarp();
