@@ -52,6 +52,13 @@ using namespace tc;
 
 __device__ int g_bwd_tc_status = 0;
 
+// Packed product of two fp32 pairs (one FMA-pipe instruction).
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 constexpr int kSoftWarps = 16;  // four per TMEM lane quarter, one per 32 queries
 constexpr int kReduceWarp = kSoftWarps;
 constexpr int kProducerWarp = kReduceWarp + 1;

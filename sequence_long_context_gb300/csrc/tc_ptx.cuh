@@ -358,11 +358,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 // Two fp32 -> two e4m3 codes (lo in the low byte): round to nearest even,
 // finite values beyond the largest code saturate to it.
 __device__ __forceinline__ uint32_t pack_e4m3(float lo, float hi) {
