@@ -286,16 +286,25 @@ def make_step(usp, w, x, cu_dev, keep=None):
     ws = usp.attn_workspace(x["q"], x["k"], cu_seqlens=cu_dev, cp=w.cp, ud=w.ud,
                             natural=True)
 
-    def step(inp):
+    def fwd(inp):
         out, lse = usp.attn_forward(inp["q"], inp["k"], inp["v"], workspace=ws, **kw)
         if keep is not None:
             keep["lse"] = lse
+        return out, lse
+
+    def bwd(inp, out, lse):
+        return list(usp.attn_backward(inp["q"], inp["k"], inp["v"], out, lse, inp["dout"],
+                                      workspace=ws, saved_exchange=True, **kw))
+
+    def step(inp):
+        out, lse = fwd(inp)
         res = [out]
         if w.backward:
-            res += list(usp.attn_backward(inp["q"], inp["k"], inp["v"], out, lse, inp["dout"],
-                                          workspace=ws, saved_exchange=True, **kw))
+            res += bwd(inp, out, lse)
         return res
 
+    # the two halves, for callers that interleave copies with them
+    step.fwd, step.bwd = fwd, bwd
     return step
 
 
@@ -578,7 +587,9 @@ def main():
     # reads its results back into pinned host memory. The copies run on their
     # own streams, double-buffered: step i+1's upload and step i-1's readback
     # overlap step i's kernels, as a training loop with a prefetching loader
-    # runs. The first upload and the last readback are inside the timed region.
+    # runs. The forward starts once q, k, v are in (dout may still be on its
+    # way) and out goes back once the forward is done. The first upload and
+    # the last readback are inside the timed region.
     e2e = None
     if not args.no_e2e:
         host = {n: x[n].cpu().pin_memory() for n in names}
@@ -600,18 +611,19 @@ def main():
             read_back = []
 
             def upload(i):
+                # one event per tensor: the forward waits for q, k, v only,
+                # the backward for dout too
                 s = i % 2
+                ready[s] = {}
                 for j, nm in enumerate(names):
                     u = ups[j % len(ups)]
                     if freed[s] is not None:
                         u.wait_event(freed[s])
                     with torch.cuda.stream(u):
                         slots[s][nm].copy_(host[nm], non_blocking=True)
-                ready[s] = []
-                for u in ups:
                     ev = torch.cuda.Event()
                     ev.record(u)
-                    ready[s].append(ev)
+                    ready[s][nm] = ev
 
             for u in ups:
                 u.wait_stream(cs)
@@ -623,18 +635,26 @@ def main():
                         ev.synchronize()
                 if i + 1 < n:
                     upload(i + 1)
-                for ev in ready[s]:
-                    cs.wait_event(ev)
-                outs = step(slots[s])
+                for nm in ("q", "k", "v"):
+                    cs.wait_event(ready[s][nm])
+                out, lse = step.fwd(slots[s])
+                fdone = torch.cuda.Event()
+                fdone.record(cs)
+                outs = [out]
+                if w.backward:
+                    cs.wait_event(ready[s]["dout"])
+                    outs += step.bwd(slots[s], out, lse)
                 done = torch.cuda.Event()
                 done.record(cs)
                 freed[s] = done
                 if outs_host[s] is None:
                     outs_host[s] = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
                                     for o in outs]
+                # the output's readback starts once the forward is done, the
+                # gradients' once the backward is
                 for j, (hb, o) in enumerate(zip(outs_host[s], outs)):
                     d = downs[j % len(downs)]
-                    d.wait_event(done)
+                    d.wait_event(fdone if j == 0 else done)
                     with torch.cuda.stream(d):
                         o.record_stream(d)
                         hb.copy_(o, non_blocking=True)
@@ -654,7 +674,9 @@ def main():
         d2h = sum(t.numel() * t.element_size() for t in outs_host[0])
         e2e = {"value": job_tflops(F["total"], world, ems), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
-               "steps": n_e2e, "copies": "double-buffered, two H2D and two D2H streams"}
+               "steps": n_e2e,
+               "copies": "double-buffered, two H2D and two D2H streams; the forward waits "
+                         "for q, k, v only, out is read back once the forward is done"}
 
     # fp8 (E4M3) forward: the inputs are quantized once, outside the timed
     # region; the forward (V transpose + attention) runs on resident codes.
