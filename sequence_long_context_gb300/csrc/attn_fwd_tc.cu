@@ -103,10 +103,11 @@ __device__ __forceinline__ int fwd_batch(const AttnParams& P, int unit) {
 // bf16 rows staged in `stage` (128-byte swizzle) and stored with TMA by the
 // first thread, LSE = (m + log2 l) ln 2. b_* are the tile's barriers;
 // nranks is the CTA order's ranks per unit (to recompute the head late).
-template <int D, int kHalfBytes, int kHalves>
+template <int D, int kHalfBytes, int kHalves, bool kSplitP>
 __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* info,
-                                             uint32_t b_info, uint32_t b_s, uint32_t b_p,
-                                             uint32_t b_o, uint32_t b_staged, uint32_t s_tm,
+                                             uint32_t b_info, uint32_t b_s, uint32_t b_ph,
+                                             uint32_t b_p, uint32_t b_o, uint32_t b_staged,
+                                             uint32_t s_tm,
                                              uint32_t o_tm, uint8_t* stage,
                                              const CUtensorMap* tm_o, int qrow0, int quarter,
                                              int lane, int nranks, volatile int* abort_flag) {
@@ -165,10 +166,33 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
     l_run *= alpha;
     const float msub = (m_run == -INFINITY) ? 0.f : m_run;
     // p = exp2(s * scale_log2 - m): scale-and-subtract and the row sum run
-    // on packed fp32 pairs (one FMA-pipe instruction per two elements)
+    // on packed fp32 pairs (one FMA-pipe instruction per two elements). P
+    // goes over S as bf16 pairs in two halves of 64 keys. kSplitP: each half
+    // is handed to the MMA warp as soon as it is written (b_ph, then b_p),
+    // so the first half's P V overlaps the second half's exponentials (the
+    // single-tile kernel, whose one softmax group leaves the tensor core
+    // idle meanwhile); otherwise P goes in one hand-off (the two-tile
+    // kernel, whose other group keeps the tensor core busy).
     const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
     const uint64_t nm2 = f2_pack(-msub, -msub);
     uint64_t ls2[4] = {0, 0, 0, 0};
+    // O_i holds PV of the previous tiles (complete: the commit that
+    // signalled S_i tracks every earlier MMA); it is rescaled to the new max
+    // before P_i V is accumulated onto it
+    auto rescale_o = [&]() {
+      if (__any_sync(0xffffffffu, need && c > 0)) {
+#pragma unroll
+        for (int oc = 0; oc < D / 32; ++oc) {
+          uint32_t o[32];
+          tmem_ld32(o_tm + 32 * oc, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            o[jj] = __float_as_uint(__uint_as_float(o[jj]) * alpha);
+          tmem_st32(o_tm + 32 * oc, o);
+        }
+      }
+    };
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
       uint32_t pk[32];
@@ -186,6 +210,13 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
         pk[j] = pack_bf16(p0, p1);
       }
       tmem_st32(s_tm + 32 * ch, pk);
+      if constexpr (kSplitP) {
+        if (ch == 0) rescale_o();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ch == 0 ? b_ph : b_p);  // one arrival per warp
+      }
     }
     {
       float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -195,25 +226,13 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
       f2_unpack(ls2[3], d0, d1);
       l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
     }
-    // O_i holds PV of the previous tiles (complete: the commit that
-    // signalled S_i tracks every earlier MMA); rescale it to the new max
-    // before P_i V is accumulated onto it.
-    if (__any_sync(0xffffffffu, need && c > 0)) {
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(o_tm + 32 * ch, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-        tmem_st32(o_tm + 32 * ch, o);
-      }
+    if constexpr (!kSplitP) {
+      rescale_o();
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_p);  // one arrival per warp
     }
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(b_p);  // one arrival per warp
     ++c;
   }
   // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2. The rows are
@@ -527,8 +546,8 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     // group i = warp / 4 takes query tile i
     const int i = warp >> 2, quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    softmax_tile<D, L::kHalfBytes, L::kHalves>(
-        P, info + i, bar(L::kInfoFull + i), bar(L::kSFull + i), bar(L::kPFull + i),
+    softmax_tile<D, L::kHalfBytes, L::kHalves, false>(
+        P, info + i, bar(L::kInfoFull + i), bar(L::kSFull + i), 0u, bar(L::kPFull + i),
         bar(L::kOFull + i), bar(L::kOStaged + i), tmem + lane_off + 128 * i,
         tmem + lane_off + 256 + D * i, sm + L::kQ + i * L::kTileBytes, &tm_o, qbase0 + i * kBM,
         quarter, lane, npairs, abort_flag);
@@ -566,7 +585,7 @@ struct Smem1 {
   static constexpr int kBar = kV + kTileBytes;
   static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 2, kVFull = 3, kVEmpty = 4,
                        kSFull = 5, kPFull = 6, kOFull = 7, kInfoFull = 8, kMmaDone = 9,
-                       kOStaged = 10, kNumBars = 11;
+                       kOStaged = 10, kPHalf = 11, kNumBars = 12;
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4
   static constexpr int kInfo = kSched + 16;                           // int2
   static constexpr int kMisc = kInfo + 16;                            // tmem base, abort
@@ -621,6 +640,7 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
     mbar_init(bar(L::kVEmpty), 1);
     mbar_init(bar(L::kSFull), 1);
     mbar_init(bar(L::kPFull), kBM / 32);    // one arrival per softmax warp
+    mbar_init(bar(L::kPHalf), kBM / 32);
     mbar_init(bar(L::kOFull), 1);
     mbar_init(bar(L::kInfoFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
@@ -738,13 +758,19 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
         }
         mma_commit(bar(L::kSFull));
         mma_commit(bar(L::kKEmpty));
-        if (!(ok = mbar_wait(bar(L::kPFull), n & 1, abort_flag, P.status))) break;
+        // the first 64 keys' P as soon as the softmax has written them
+        if (!(ok = mbar_wait(bar(L::kPHalf), n & 1, abort_flag, P.status))) break;
         if (!(ok = mbar_wait(bar(L::kVFull), n & 1, abort_flag, P.status))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
+        for (int kk = 0; kk < kBN / 32; ++kk)
           mma_ts(o_tm, s_tm + kk * 8, sdesc_add(dv0, kk * 2048), kIdPV,
                  (n > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = mbar_wait(bar(L::kPFull), n & 1, abort_flag, P.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = kBN / 32; kk < kBN / 16; ++kk)
+          mma_ts(o_tm, s_tm + kk * 8, sdesc_add(dv0, kk * 2048), kIdPV, 1u);
         mma_commit(bar(L::kVEmpty));
         ++n;
       }
@@ -760,8 +786,9 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
     // one query row per thread, as one group of the two-tile kernel
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    softmax_tile<D, L::kHalfBytes, L::kHalves>(
-        P, info, bar(L::kInfoFull), bar(L::kSFull), bar(L::kPFull), bar(L::kOFull),
+    softmax_tile<D, L::kHalfBytes, L::kHalves, true>(
+        P, info, bar(L::kInfoFull), bar(L::kSFull), bar(L::kPHalf), bar(L::kPFull),
+        bar(L::kOFull),
         bar(L::kOStaged), tmem + lane_off, tmem + lane_off + 128, sm + L::kQ, &tm_o, qbase,
         quarter, lane, ntiles, abort_flag);
   }
