@@ -9,18 +9,18 @@
 // is folded into the running partial (row max m, row sum l, O accumulator),
 // which is the unnormalised form of a merged (O, LSE) partial.
 //
-// One CTA owns two 128-row query tiles of one (batch, head) of the same
-// ring rank. Roles (320 threads):
-//   warps 0-3   softmax group 0: one query row of tile 0 per thread
-//   warps 4-7   softmax group 1: one query row of tile 1 per thread
-//   warp  8     producer: classifies key tiles (empty / full / masked) and
-//               streams K and V tiles with TMA into two-slot rings
-//   warp  9     MMA issuer (one thread) and owner of the tensor memory
-// Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128),
-// overwritten in place by P_i (bf16 pairs, first 64 columns) which feeds
-// O_i += P_i V as the A operand from tensor memory; O_i at 256 + D i.
-// The two tiles ping-pong: while one group turns S into P, the tensor core
-// runs the other tile's P V and next Q K^T.
+// One CTA owns one 128-row query tile of one (batch, head); two CTAs share
+// an SM. Roles (192 threads):
+//   warps 0-3   softmax: one query row per thread
+//   warp  4     producer: classifies key tiles (empty / full / masked) and
+//               streams K and V tiles with TMA, one slot each
+//   warp  5     MMA issuer (one thread) and owner of the CTA's tensor memory
+// Tensor memory (256 columns per CTA): S = Q K^T at [0, 128), overwritten in
+// place by P (bf16 pairs) which feeds O += P V as the A operand from tensor
+// memory; O at [128, 128 + D). P goes to the MMA warp in two halves of 64
+// keys, so the first half's P V runs while the second half's exponentials
+// are computed, and the two CTAs of an SM interleave their products on the
+// tensor core.
 // Masks are resolved per 128x128 tile: empty tiles are never loaded, full
 // tiles run without any mask arithmetic, masked tiles test each element
 // against the row's visible interval. The running max is only moved (and O
@@ -45,48 +45,13 @@ __device__ int g_fwd_tc_status = 0;
 
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per tile
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
 constexpr int kEmpty = kClsEmpty, kMasked = kClsMasked;
 constexpr int kEnd = -1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// Depth of the V ring (the K ring has two slots). A third V slot fits the
-// shared memory but measured no faster.
-constexpr int kVSlots = 2;
 constexpr float kLn2 = 0.6931471805599453f;
-
-template <int D>
-struct Smem {
-  static constexpr int kHalves = D / 64;              // 128-byte swizzle rows
-  static constexpr int kTileBytes = kBM * D * 2;       // one 128 x D bf16 tile
-  static constexpr int kHalfBytes = kBM * 128;         // 128 rows x 128 bytes
-  // offsets from the 1024-aligned base
-  static constexpr int kQ = 0;                          // 2 query tiles
-  static constexpr int kK = kQ + 2 * kTileBytes;        // 2 key slots
-  static constexpr int kV = kK + 2 * kTileBytes;        // kVSlots value slots
-  static constexpr int kBar = kV + kVSlots * kTileBytes;
-  // barriers (8 bytes each)
-  static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5,
-                       kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots,
-                       kPFull = kSFull + 2, kOFull = kPFull + 2, kInfoFull = kOFull + 2,
-                       kMmaDone = kInfoFull + 2, kOStaged = kMmaDone + 1,
-                       kNumBars = kOStaged + 2;
-  static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
-  static constexpr int kInfo = kSched + 32;             // int2 x 2
-  static constexpr int kMisc = kInfo + 16;              // tmem base, abort
-  static constexpr int kBytes = kMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;          // alignment slack
-  static_assert(kSched % 16 == 0 && kInfo % 8 == 0, "vector accesses need alignment");
-  static_assert(kK % 1024 == 0 && kV % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
-};
 
 // CTA order: units are query heads ordered (kv head, batch, query head of
 // the group), so a batch of consecutive units shares K/V.
-__device__ __forceinline__ CtaOrder fwd_order(const AttnParams& P, int npairs) {
-  return batched_order(blockIdx.x, P.Hq * P.Bt, npairs, P.unit_batch);
-}
 __device__ __forceinline__ int fwd_head(const AttnParams& P, int unit) {
   return unit / (P.G * P.Bt) * P.G + unit % P.G;
 }
@@ -99,11 +64,12 @@ __device__ __forceinline__ int fwd_batch(const AttnParams& P, int unit) {
 // 2^(S scale log2e - m) written over S as bf16 pairs (the A operand of P V),
 // the running max m moved only when it grows by more than 2^8 (and O
 // rescaled then; exact, since O / l and m + log l do not depend on which m
-// was used), the row sum accumulated on packed pairs. Epilogue: O / l as
-// bf16 rows staged in `stage` (128-byte swizzle) and stored with TMA by the
-// first thread, LSE = (m + log2 l) ln 2. b_* are the tile's barriers;
-// nranks is the CTA order's ranks per unit (to recompute the head late).
-template <int D, int kHalfBytes, int kHalves, bool kSplitP>
+// was used), the row sum accumulated on packed pairs; P is handed over in
+// two halves (b_ph, then b_p). Epilogue: O / l as bf16 rows staged in
+// `stage` (128-byte swizzle) and stored with TMA by the first thread, LSE =
+// (m + log2 l) ln 2. b_* are the tile's barriers; nranks is the CTA order's
+// ranks per unit (to recompute the head late).
+template <int D, int kHalfBytes, int kHalves>
 __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* info,
                                              uint32_t b_info, uint32_t b_s, uint32_t b_ph,
                                              uint32_t b_p, uint32_t b_o, uint32_t b_staged,
@@ -167,12 +133,9 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
     const float msub = (m_run == -INFINITY) ? 0.f : m_run;
     // p = exp2(s * scale_log2 - m): scale-and-subtract and the row sum run
     // on packed fp32 pairs (one FMA-pipe instruction per two elements). P
-    // goes over S as bf16 pairs in two halves of 64 keys. kSplitP: each half
-    // is handed to the MMA warp as soon as it is written (b_ph, then b_p),
-    // so the first half's P V overlaps the second half's exponentials (the
-    // single-tile kernel, whose one softmax group leaves the tensor core
-    // idle meanwhile); otherwise P goes in one hand-off (the two-tile
-    // kernel, whose other group keeps the tensor core busy).
+    // goes over S as bf16 pairs in two halves of 64 keys, each handed to the
+    // MMA warp as soon as it is written (b_ph, then b_p), so the first
+    // half's P V overlaps the second half's exponentials.
     const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
     const uint64_t nm2 = f2_pack(-msub, -msub);
     uint64_t ls2[4] = {0, 0, 0, 0};
@@ -210,13 +173,11 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
         pk[j] = pack_bf16(p0, p1);
       }
       tmem_st32(s_tm + 32 * ch, pk);
-      if constexpr (kSplitP) {
-        if (ch == 0) rescale_o();
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ch == 0 ? b_ph : b_p);  // one arrival per warp
-      }
+      if (ch == 0) rescale_o();  // before the first half goes
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ch == 0 ? b_ph : b_p);  // one arrival per warp
     }
     {
       float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -225,13 +186,6 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
       f2_unpack(ls2[2], c0, c1);
       f2_unpack(ls2[3], d0, d1);
       l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-    }
-    if constexpr (!kSplitP) {
-      rescale_o();
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_p);  // one arrival per warp
     }
     ++c;
   }
@@ -292,290 +246,18 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
   }
 }
 
-// 10 warps: three share a 16K-register sub-partition, so <= 168 each.
-template <int D>
-__global__ void __maxnreg__(168)
-attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v,
-                   const __grid_constant__ CUtensorMap tm_o) {
-  using L = Smem<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(sm);
-  auto bar = [&](int i) { return sbase + L::kBar + 8 * i; };
-  int4* sched = reinterpret_cast<int4*>(sm + L::kSched);
-  int2* info = reinterpret_cast<int2*>(sm + L::kInfo);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int npairs = P.S / (2 * kBM);
-  const CtaOrder ord = fwd_order(P, npairs);
-  const int pair = qpair_for_rank(P, ord.rank, npairs);
-  const int h = fwd_head(P, ord.unit), bt = fwd_batch(P, ord.unit);
-  const int g = h / P.G;
-  const int qbase0 = pair * 2 * kBM;          // permuted row of tile 0
-  const int rho = qbase0 / P.shard;           // ring rank of both tiles
-
-  // The producer thread sets up the barriers and starts the query tiles'
-  // load before the CTA-wide barrier, so the load overlaps the set-up.
-  if (warp == kProducerWarp && lane == 0) {
-    mbar_init(bar(L::kQFull), 1);
-    for (int s = 0; s < kVSlots; ++s) {
-      mbar_init(bar(L::kVFull + s), 1);
-      mbar_init(bar(L::kVEmpty + s), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kKFull + s), 1);
-      mbar_init(bar(L::kKEmpty + s), 1);
-      mbar_init(bar(L::kSFull + s), 1);
-      mbar_init(bar(L::kPFull + s), kBM / 32);  // one arrival per softmax warp
-      mbar_init(bar(L::kOFull + s), 1);
-      mbar_init(bar(L::kInfoFull + s), 1);
-      mbar_init(bar(L::kOStaged + s), kBM / 32);  // one arrival per softmax warp
-    }
-    mbar_init(bar(L::kMmaDone), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-    tma_prefetch(&tm_q);
-    tma_prefetch(&tm_k);
-    tma_prefetch(&tm_v);
-    mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
-    for (int i = 0; i < 2; ++i) {
-      const TensorPos t = tensor_pos(P, h, qbase0 + i * kBM, bt, P.Hq);
-      for (int hf = 0; hf < L::kHalves; ++hf)
-        tma_load_4d(sbase + L::kQ + i * L::kTileBytes + hf * L::kHalfBytes, &tm_q,
-                    bar(L::kQFull), hf * 64, t.h, t.row, t.b);
-    }
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(sbase + L::kMisc, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const TileSpan q0 = tile_span(P, qbase0), q1 = tile_span(P, qbase0 + kBM);
-      const KeyWindows w0 = key_windows(P, q0), w1 = key_windows(P, q1);
-      const PosRange band = {min(w0.band.lo, w1.band.lo), max(w0.band.hi, w1.band.hi)};
-      const PosRange sinks = {min(w0.sink.lo, w1.sink.lo), max(w0.sink.hi, w1.sink.hi)};
-      int n = 0;   // key tiles with K and V issued
-      int nk = 0;  // key tiles with K issued (n or n + 1)
-      bool ok = true;
-      // packed sequences of the two query tiles (fixed) and of the last key
-      // tile (the next one's first guess)
-      const SegInfo sq0 = seg_info(P, q0), sq1 = seg_info(P, q1, sq0.last);
-      int khint = sq0.first;
-      // one key tile: classified for both query tiles, loaded unless empty
-      // for both
-      auto visit = [&](int kt) {
-        const TileSpan ks = tile_span(P, kt * kBN);
-        const bool out0 = disjoint(ks, w0.band) && disjoint(ks, w0.sink);
-        const bool out1 = disjoint(ks, w1.band) && disjoint(ks, w1.sink);
-        if (out0 && out1) return;
-        const SegInfo sk = seg_info(P, ks, khint);
-        khint = sk.last;
-        const int c0 = out0 ? kEmpty : classify(P, q0, sq0, ks, sk);
-        const int c1 = out1 ? kEmpty : classify(P, q1, sq1, ks, sk);
-        if (c0 == kEmpty && c1 == kEmpty) return;
-        const int slot = n & 1, use = n >> 1;
-        if (use >= 1 && !(ok = mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1,
-                                         abort_flag, P.status)))
-          return;
-        sched[slot] = make_int4(kt, c0, c1, 0);
-        const TensorPos kv = tensor_pos(P, g, kt * kBN, bt, P.Hkv);
-        mbar_expect_tx(bar(L::kKFull + slot), L::kTileBytes);
-        for (int hf = 0; hf < L::kHalves; ++hf)
-          tma_load_4d(sbase + L::kK + slot * L::kTileBytes + hf * L::kHalfBytes,
-                      &tm_k, bar(L::kKFull + slot), hf * 64, kv.h, kv.row, kv.b);
-        ++nk;
-        const int vslot = n % kVSlots, vuse = n / kVSlots;
-        if (vuse >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + vslot), (vuse - 1) & 1,
-                                          abort_flag, P.status)))
-          return;
-        mbar_expect_tx(bar(L::kVFull + vslot), L::kTileBytes);
-        for (int hf = 0; hf < L::kHalves; ++hf)
-          tma_load_4d(sbase + L::kV + vslot * L::kTileBytes + hf * L::kHalfBytes,
-                      &tm_v, bar(L::kVFull + vslot), hf * 64, kv.h, kv.row, kv.b);
-        ++n;
-      };
-      for (int s = 0; s < P.cp && ok; ++s) {
-        const int kap = (rho - s + P.cp) % P.cp;
-        // only the runs of the shard that can hold visible keys are visited:
-        // the sink tokens' tiles first, then the band's (without those)
-        TileRun sr[2], br[2];
-        const int nsr = sinks.lo <= sinks.hi ? shard_runs(P, kap, sinks, sr) : 0;
-        const int nbr = shard_runs(P, kap, band, br);
-        for (int ri = 0; ri < nsr && ok; ++ri)
-          for (int kt = sr[ri].begin; kt < sr[ri].end && ok; ++kt) visit(kt);
-        for (int ri = 0; ri < nbr && ok; ++ri)
-          for (int kt = br[ri].begin; kt < br[ri].end && ok; ++kt) {
-            bool seen = false;
-            for (int rj = 0; rj < nsr; ++rj) seen |= kt >= sr[rj].begin && kt < sr[rj].end;
-            if (!seen) visit(kt);
-          }
-      }
-      if (ok) {
-        const int slot = n & 1, use = n >> 1;
-        if (use < 1 || mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1, abort_flag,
-                                 P.status)) {
-          sched[slot] = make_int4(kEnd, 0, 0, 0);
-          mbar_arrive(bar(L::kKFull + slot));
-        }
-        // tail: every issued copy has been consumed before the CTA may exit
-        for (int m = (n >= kVSlots ? n - kVSlots : 0); m < n; ++m) {
-          const int sl = m % kVSlots, us = m / kVSlots;
-          if (!mbar_wait(bar(L::kVEmpty + sl), us & 1, abort_flag, P.status)) break;
-        }
-      }
-      if (*abort_flag) {
-        // aborted: let the copies already issued land before the CTA exits
-        mbar_wait_drain(bar(L::kQFull), 0);
-        for (int m = (nk >= 2 ? nk - 2 : 0); m < nk; ++m)
-          mbar_wait_drain(bar(L::kKFull + (m & 1)), (m >> 1) & 1);
-        for (int m = (n >= kVSlots ? n - kVSlots : 0); m < n; ++m)
-          mbar_wait_drain(bar(L::kVFull + m % kVSlots), (m / kVSlots) & 1);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // Issue order per key tile n (e0/e1: tile n is non-empty for query tile
-    // 0/1): QK0(n), PV1(previous tile of query tile 1), release V slot of
-    // tile n-1, QK1(n), release K slot of n, PV0(n). QK_i(n) is always issued
-    // after PV_i of i's previous tile, so S_i may overwrite P_i in place.
-    if (lane == 0) {
-      constexpr uint32_t kIdQK = idesc_bf16_f32(kBM, kBN, 0, 0);
-      constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, 0, 1);
-      const uint32_t s_tm[2] = {tmem, tmem + 128};
-      const uint32_t o_tm[2] = {tmem + 256, tmem + 256 + D};
-      int cnt[2] = {0, 0};  // QK issued per query tile
-      // operand descriptors, built once: the first query tile, the first K
-      // slot and the first V slot (the others are whole tiles further on)
-      const uint64_t dq0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
-      const uint64_t dk0 = sdesc_sw128(sbase + L::kK, 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(sbase + L::kV, L::kHalfBytes, 1024);
-      bool ok = mbar_wait(bar(L::kQFull), 0, abort_flag, P.status);
-      auto qk = [&](int i, int slot) {
-        const uint64_t qd = sdesc_add(dq0, i * L::kTileBytes);
-        const uint64_t kd = sdesc_add(dk0, slot * L::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          mma_ss(s_tm[i], sdesc_add(qd, off), sdesc_add(kd, off), kIdQK, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kSFull + i));
-        ++cnt[i];
-      };
-      // O_i (+)= P_i V(slot); waits for P_i of the latest QK_i and for V
-      // (slot, use: the V ring's).
-      auto pv = [&](int i, int slot, int use, int first) -> bool {
-        if (!mbar_wait(bar(L::kPFull + i), (cnt[i] - 1) & 1, abort_flag, P.status))
-          return false;
-        if (!mbar_wait(bar(L::kVFull + slot), use & 1, abort_flag, P.status))
-          return false;
-        tc_fence_after();
-        const uint64_t vd = sdesc_add(dv0, slot * L::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(o_tm[i], s_tm[i] + kk * 8, sdesc_add(vd, kk * 2048), kIdPV,
-                 (first && kk == 0) ? 0u : 1u);
-        return true;
-      };
-      int n = 0;
-      int first[2] = {1, 1};
-      int pend_slot = -1, pend_use = 0, pend_first = 0;  // PV1 still to issue
-      int prev_slot = -1;                                // V slot of tile n-1
-      while (ok) {
-        const int slot = n & 1, use = n >> 1;            // K slot
-        const int vslot = n % kVSlots, vuse = n / kVSlots;
-        if (!(ok = mbar_wait(bar(L::kKFull + slot), use & 1, abort_flag, P.status)))
-          break;
-        const int4 e = sched[slot];
-        if (e.x == kEnd) break;
-        tc_fence_after();
-        const bool e0 = e.y != kEmpty, e1 = e.z != kEmpty;
-        if (e0) {
-          info[0] = make_int2(e.x, e.y);
-          mbar_arrive(bar(L::kInfoFull + 0));
-          qk(0, slot);
-        }
-        if (pend_slot >= 0) {
-          if (!(ok = pv(1, pend_slot, pend_use, pend_first))) break;
-          pend_slot = -1;
-        }
-        if (prev_slot >= 0) mma_commit(bar(L::kVEmpty + prev_slot));
-        if (e1) {
-          info[1] = make_int2(e.x, e.z);
-          mbar_arrive(bar(L::kInfoFull + 1));
-          qk(1, slot);
-        }
-        mma_commit(bar(L::kKEmpty + slot));
-        if (e0) {
-          if (!(ok = pv(0, vslot, vuse, first[0]))) break;
-          first[0] = 0;
-        }
-        if (e1) {
-          pend_slot = vslot;
-          pend_use = vuse;
-          pend_first = first[1];
-          first[1] = 0;
-        }
-        prev_slot = vslot;
-        ++n;
-      }
-      if (ok && pend_slot >= 0) ok = pv(1, pend_slot, pend_use, pend_first);
-      if (ok && prev_slot >= 0) mma_commit(bar(L::kVEmpty + prev_slot));
-      for (int i = 0; i < 2; ++i) {
-        mma_commit(bar(L::kOFull + i));
-        info[i] = make_int2(kEnd, 0);
-        mbar_arrive(bar(L::kInfoFull + i));
-      }
-      // nothing of ours may still run on the tensor core when TMEM is freed
-      mma_commit(bar(L::kMmaDone));
-      mbar_wait_drain(bar(L::kMmaDone), 0);
-    }
-  } else {
-    // ------------------------------------------------------------ softmax
-    // group i = warp / 4 takes query tile i
-    const int i = warp >> 2, quarter = warp & 3;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    softmax_tile<D, L::kHalfBytes, L::kHalves, false>(
-        P, info + i, bar(L::kInfoFull + i), bar(L::kSFull + i), 0u, bar(L::kPFull + i),
-        bar(L::kOFull + i), bar(L::kOStaged + i), tmem + lane_off + 128 * i,
-        tmem + lane_off + 256 + D * i, sm + L::kQ + i * L::kTileBytes, &tm_o, qbase0 + i * kBM,
-        quarter, lane, npairs, abort_flag);
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
-}
-
 // ---------------------------------------------------------------------------
-// One query tile per CTA, two CTAs per SM. For windowed problems (and
-// packed sequences) a query tile meets few key tiles, and a CTA's fixed
-// costs (set-up, the Q load, the first key tile, the epilogue) are a large
-// share of its time. This variant
-// takes half the tensor memory (S at [0,128), overwritten by P, O at
-// [128, 128+D)) and under half the shared memory (one Q tile, one K and one
-// V slot), so the SM runs two CTAs: one's start and end overlap the other's
-// loop, and their Q K^T and P V products interleave on the tensor core as
-// the two query tiles of the two-tile kernel do. Same ring schedule, tile
-// classes, masks, lazy rescale and epilogue as that kernel.
-constexpr int kThreads1 = 192;      // softmax warps 0-3, producer 4, MMA 5
-constexpr int kProducerWarp1 = 4;
-constexpr int kMmaWarp1 = 5;
+// The kernel. One query tile per CTA (S at [0,128) of the CTA's 256 tensor
+// memory columns, overwritten by P, O at [128, 128+D); one Q tile, one K and
+// one V slot of shared memory), so the SM runs two CTAs: one's start and end
+// overlap the other's loop, and their Q K^T and P V products interleave on
+// the tensor core.
+constexpr int kThreads = 192;      // softmax warps 0-3, producer 4, MMA 5
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
 
 template <int D>
-struct Smem1 {
+struct Smem {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kBM * D * 2;
   static constexpr int kHalfBytes = kBM * 128;
@@ -606,12 +288,12 @@ __device__ __forceinline__ int qtile_for_rank(const AttnParams& P, int r, int nt
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads1, 2)
-attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(kThreads, 2)
+attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o) {
-  using L = Smem1<D>;
+  using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -632,7 +314,7 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
   const int rho = qbase / P.shard;       // its ring rank
 
   // the producer thread sets up the barriers and starts the Q load
-  if (warp == kProducerWarp1 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     mbar_init(bar(L::kQFull), 1);
     mbar_init(bar(L::kKFull), 1);
     mbar_init(bar(L::kKEmpty), 1);
@@ -656,7 +338,7 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
       tma_load_4d(sbase + L::kQ + hf * L::kHalfBytes, &tm_q, bar(L::kQFull), hf * 64, t.h,
                   t.row, t.b);
   }
-  if (warp == kMmaWarp1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sbase + L::kMisc, 256);
     tmem_relinquish();
   }
@@ -665,7 +347,7 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == kProducerWarp1) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const TileSpan q0 = tile_span(P, qbase);
@@ -730,7 +412,7 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
         if (n >= 1) mbar_wait_drain(bar(L::kVFull), (n - 1) & 1);
       }
     }
-  } else if (warp == kMmaWarp1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // Per key tile n: S = Q K^T (then the K slot is free), P V once the
     // softmax has written P over S (then the V slot is free). The next
@@ -783,10 +465,10 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // one query row per thread, as one group of the two-tile kernel
+    // one query row per thread
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    softmax_tile<D, L::kHalfBytes, L::kHalves, true>(
+    softmax_tile<D, L::kHalfBytes, L::kHalves>(
         P, info, bar(L::kInfoFull), bar(L::kSFull), bar(L::kPHalf), bar(L::kPFull),
         bar(L::kOFull),
         bar(L::kOStaged), tmem + lane_off, tmem + lane_off + 128, sm + L::kQ, &tm_o, qbase,
@@ -796,7 +478,7 @@ attn_fwd_tc1_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp1) tmem_dealloc(tmem, 256);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 256);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -850,7 +532,6 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
       !make_map(&mv, P.v, Bm, P.S, P.Hkv * hm, D, P.qkv_tok) ||
       !make_map(&mo, P.o, Bm, P.S, P.Hq * hm, D))
     return USP_ERR_CUDA;  // detail recorded by make_map
-  const int smem = Smem<D>::kAlloc;
   static int* status = nullptr;
   if (status == nullptr) {
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_fwd_tc_status);
@@ -858,40 +539,16 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   }
   AttnParams Pk = P;
   Pk.status = status;
-  // L2 batches: enough query-tile pairs for about eight waves of CTAs, in
-  // whole GQA groups (at S=8K with 32 heads of 32 pairs, 40 heads per batch
-  // ran 5 % faster than 10; longer sequences are insensitive)
-  {
-    const int npairs = P.S / (2 * kBM);
-    int per = (8 * sm_count() + npairs - 1) / npairs;
-    per = (per + P.G - 1) / P.G * P.G;
-    Pk.unit_batch = per < P.Hq * P.Bt ? per : P.Hq * P.Bt;
-  }
-  // windowed problems and packed sequences (short key ranges per query
-  // tile: measured 13 % faster for the S=8K window of 1000, 3.6 % for the
-  // 128K packed batch; 2 % slower on the dense S=32K ring): one query tile
-  // per CTA, two CTAs per SM, batches of about eight waves of those
-  if (P.window > 0 || P.cu != nullptr) {
-    const int ntiles = P.S / kBM;
-    int per = (16 * sm_count() + ntiles - 1) / ntiles;
-    per = (per + P.G - 1) / P.G * P.G;
-    Pk.unit_batch = per < P.Hq * P.Bt ? per : P.Hq * P.Bt;
-    const int smem1 = Smem1<D>::kAlloc;
-    static bool attr1_set = false;
-    if (!attr1_set) {
-      cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc1_kernel<D>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem1);
-      if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(smem)", e);
-      attr1_set = true;
-    }
-    const long long blocks1 = (long long)ntiles * P.Hq * P.Bt;
-    {
-      ProfScope ps(st, "attn_fwd_tc");
-      attn_fwd_tc1_kernel<D><<<(unsigned)blocks1, kThreads1, smem1, st>>>(Pk, mq, mk, mv, mo);
-    }
-    note_launch();
-    return check_launch();
-  }
+  // L2 batches of about eight waves of CTAs (two per SM), in whole GQA
+  // groups. One query tile per CTA on every problem: on dense rings this ran
+  // 8-11 % faster than a kernel with two query tiles per CTA ping-ponging on
+  // one tensor core (S=32K 6.57 -> 5.93 ms), and more on windowed problems and
+  // packed sequences (short key ranges per query tile).
+  const int ntiles = P.S / kBM;
+  int per = (16 * sm_count() + ntiles - 1) / ntiles;
+  per = (per + P.G - 1) / P.G * P.G;
+  Pk.unit_batch = per < P.Hq * P.Bt ? per : P.Hq * P.Bt;
+  const int smem = Smem<D>::kAlloc;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
@@ -899,7 +556,7 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
     if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(smem)", e);
     attr_set = true;
   }
-  const long long blocks = (long long)(P.S / (2 * kBM)) * P.Hq * P.Bt;
+  const long long blocks = (long long)ntiles * P.Hq * P.Bt;
   {
     ProfScope ps(st, "attn_fwd_tc");
     attn_fwd_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(Pk, mq, mk, mv, mo);
