@@ -26,7 +26,8 @@
 //  * q_descale * k_descale is folded into the softmax scale; v_descale
 //    multiplies O in the epilogue.
 // Tensor memory (512 columns): S_i at [128 i, 128 i + 128), O_i at
-// 256 + 128 i. The two query tiles ping-pong as in the bf16 kernel.
+// 256 + 128 i. The two query tiles ping-pong on the tensor core: while one
+// group turns S into P, the other tile's P V and next Q K^T run.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
