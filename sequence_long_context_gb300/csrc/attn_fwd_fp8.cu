@@ -9,25 +9,26 @@
 // with the log-sum-exp rule), computed on 8-bit operands. The real value of
 // a code c of a tensor with descale d is e4m3(c) * d.
 //
-// One CTA owns two 128-row query tiles of one (batch, head) of one ring
-// rank; roles as in the bf16 forward (320 threads):
-//   warps 0-3 / 4-7  softmax groups of query tile 0 / 1, one row per thread
-//   warp  8          producer: classifies key tiles, streams K and V^T tiles
-//   warp  9          MMA issuer and tensor-memory owner
+// One CTA owns one 128-row query tile of one (batch, head) of one ring rank
+// and two CTAs share an SM; roles (192 threads):
+//   warps 0-3  softmax, one query row per thread
+//   warp  4    producer: classifies key tiles, streams K and V^T tiles
+//   warp  5    MMA issuer and owner of the CTA's tensor memory
 // What the 8-bit operands change:
 //  * Q and K tiles are 128 tokens x 128 codes, one 128-byte swizzle row per
 //    token. V is read transposed ([d][key], keys contiguous, written by the
 //    transpose pre-pass), so both products take K-major operands:
-//    S_i = Q_i K^T and O_i += P_i (V^T)^T, 32 K elements per instruction.
-//  * P_i goes to shared memory as e4m3 codes of 16 p, a 128 x 128 K-major
+//    S = Q K^T and O += P (V^T)^T, 32 K elements per instruction.
+//  * P goes to shared memory as e4m3 codes of 16 p, a 128 x 128 K-major
 //    tile. The running max moves whenever the row max grows by more than 2^4,
 //    so p <= 2^4 and 16 p <= 256, below the largest code (448); the row sum
 //    l accumulates 16 p in fp32 and the scale cancels in O = sum(16 p v) / l.
+//  * Since P does not go back into tensor memory, S is free as soon as the
+//    softmax has loaded it: the next key tile's Q K^T is issued then, and
+//    runs while this tile's exponentials are computed.
 //  * q_descale * k_descale is folded into the softmax scale; v_descale
 //    multiplies O in the epilogue.
-// Tensor memory (512 columns): S_i at [128 i, 128 i + 128), O_i at
-// 256 + 128 i. The two query tiles ping-pong on the tensor core: while one
-// group turns S into P, the other tile's P V and next Q K^T run.
+// Tensor memory (256 columns per CTA): S at [0, 128), O at [128, 256).
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -46,49 +47,54 @@ __device__ int g_fwd_fp8_status = 0;
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr int kD = 128;   // head dim (one 128-byte swizzle row of codes)
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
 constexpr int kEmpty = kClsEmpty, kMasked = kClsMasked;
 constexpr int kEnd = -1;
-constexpr int kVSlots = 2;
 constexpr float kRescaleThreshold = 4.0f;  // log2 units; bounds p by 2^4
 constexpr float kPLog2 = 4.0f;             // P codes hold 2^4 p
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct Smem8 {
   static constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 one-byte codes
-  static constexpr int kQ = 0;                  // 2 query tiles
-  static constexpr int kK = kQ + 2 * kTileBytes;             // 2 key slots
-  static constexpr int kV = kK + 2 * kTileBytes;             // kVSlots V^T slots
-  static constexpr int kP = kV + kVSlots * kTileBytes;       // 2 P tiles
-  static constexpr int kBar = kP + 2 * kTileBytes;
-  static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5,
-                       kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots,
-                       kPFull = kSFull + 2, kOFull = kPFull + 2, kInfoFull = kOFull + 2,
-                       kMmaDone = kInfoFull + 2, kOStaged = kMmaDone + 1,
-                       kNumBars = kOStaged + 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;       // 2 key slots
+  static constexpr int kV = kK + 2 * kTileBytes;   // 2 V^T slots
+  static constexpr int kP = kV + 2 * kTileBytes;   // the P tile
+  static constexpr int kBar = kP + kTileBytes;
+  // kSFree: the softmax has loaded S (the next Q K^T may overwrite it);
+  // kPFree: the P V that read the P tile (and updated O) is done
+  static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7,
+                       kSFull = 9, kSFree = 10, kPFull = 11, kPFree = 12, kOFull = 13,
+                       kInfoFull = 14, kMmaDone = 15, kOStaged = 16, kNumBars = 17;
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4 x 2
-  static constexpr int kInfo = kSched + 32;                            // int2 x 2
+  static constexpr int kInfo = kSched + 32;                            // int2
   static constexpr int kMisc = kInfo + 16;                             // tmem base, abort
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // alignment slack
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kP % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
-  static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
+  static_assert(2 * kAlloc <= 232448, "two CTAs must fit one SM's shared memory");
 };
 
-__device__ __forceinline__ CtaOrder fwd_order(const AttnParams& P, int npairs) {
-  return batched_order(blockIdx.x, P.Hq * P.Bt, npairs, P.unit_batch);
-}
 __device__ __forceinline__ int fwd_head(const AttnParams& P, int unit) {
   return unit / (P.G * P.Bt) * P.G + unit % P.G;
 }
 __device__ __forceinline__ int fwd_batch(const AttnParams& P, int unit) {
   return (unit / P.G) % P.Bt;
 }
+// Query tiles (128 rows), heaviest first for causal dense problems.
+__device__ __forceinline__ int qtile_for_rank(const AttnParams& P, int r, int ntiles) {
+  if (!P.causal || P.cu != nullptr) return r;
+  if (P.layout == kStripe) {
+    const int tpr = P.shard / kBM;
+    return (r % P.cp) * tpr + (tpr - 1 - r / P.cp);
+  }
+  return permuted_of(P, (ntiles - 1 - r) * kBM) / kBM;
+}
 
-__global__ void __maxnreg__(168)
+__global__ void __launch_bounds__(kThreads, 2)
 attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
                     const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -106,35 +112,41 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int npairs = P.S / (2 * kBM);
-  const CtaOrder ord = fwd_order(P, npairs);
-  const int pair = qpair_for_rank(P, ord.rank, npairs);
+  const int ntiles = P.S / kBM;
+  const CtaOrder ord = batched_order(blockIdx.x, P.Hq * P.Bt, ntiles, P.unit_batch);
+  const int qt = qtile_for_rank(P, ord.rank, ntiles);
   const int h = fwd_head(P, ord.unit), bt = fwd_batch(P, ord.unit);
   const int g = h / P.G;
-  const int qbase0 = pair * 2 * kBM;
-  const int rho = qbase0 / P.shard;
+  const int qbase = qt * kBM;        // permuted row of the tile
+  const int rho = qbase / P.shard;   // its ring rank
 
-  if (threadIdx.x == 0) {
+  // the producer thread sets up the barriers and starts the Q load
+  if (warp == kProducerWarp && lane == 0) {
     mbar_init(bar(L::kQFull), 1);
-    for (int s = 0; s < kVSlots; ++s) {
-      mbar_init(bar(L::kVFull + s), 1);
-      mbar_init(bar(L::kVEmpty + s), 1);
-    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kKEmpty + s), 1);
-      mbar_init(bar(L::kSFull + s), 1);
-      mbar_init(bar(L::kPFull + s), kBM / 32);
-      mbar_init(bar(L::kOFull + s), 1);
-      mbar_init(bar(L::kInfoFull + s), 1);
-      mbar_init(bar(L::kOStaged + s), kBM / 32);
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
     }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kSFree), kBM / 32);   // one arrival per softmax warp
+    mbar_init(bar(L::kPFull), kBM / 32);   // one arrival per softmax warp
+    mbar_init(bar(L::kPFree), 1);
+    mbar_init(bar(L::kOFull), 1);
+    mbar_init(bar(L::kInfoFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
+    mbar_init(bar(L::kOStaged), kBM / 32);  // one arrival per softmax warp
     *abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch(&tm_q);
+    tma_prefetch(&tm_k);
+    tma_prefetch(&tm_vt);
+    mbar_expect_tx(bar(L::kQFull), L::kTileBytes);
+    tma_load_4d(sbase + L::kQ, &tm_q, bar(L::kQFull), 0, h, qbase, bt);
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(sbase + L::kMisc, 512);
+    tmem_alloc(sbase + L::kMisc, 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -144,58 +156,46 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Key tiles in ring order, classified for the query tile and loaded
+    // unless empty: K and V^T through two-slot rings, freed by the tile's
+    // Q K^T and P V.
     if (lane == 0) {
-      tma_prefetch(&tm_q);
-      tma_prefetch(&tm_k);
-      tma_prefetch(&tm_vt);
-      const TileSpan q0 = tile_span(P, qbase0), q1 = tile_span(P, qbase0 + kBM);
-      const KeyWindows w0 = key_windows(P, q0), w1 = key_windows(P, q1);
-      const PosRange band = {min(w0.band.lo, w1.band.lo), max(w0.band.hi, w1.band.hi)};
-      const PosRange sinks = {min(w0.sink.lo, w1.sink.lo), max(w0.sink.hi, w1.sink.hi)};
-      mbar_expect_tx(bar(L::kQFull), 2 * L::kTileBytes);
-      for (int i = 0; i < 2; ++i)
-        tma_load_4d(sbase + L::kQ + i * L::kTileBytes, &tm_q, bar(L::kQFull), 0, h,
-                    qbase0 + i * kBM, bt);
+      const TileSpan q0 = tile_span(P, qbase);
+      const KeyWindows w0 = key_windows(P, q0);
+      const SegInfo sq0 = seg_info(P, q0);
+      int khint = sq0.first;
       int n = 0, nk = 0;
       bool ok = true;
-      // packed sequences of the two query tiles (fixed) and of the last key
-      // tile (the next one's first guess)
-      const SegInfo sq0 = seg_info(P, q0), sq1 = seg_info(P, q1, sq0.last);
-      int khint = sq0.first;
       auto visit = [&](int kt) {
         const TileSpan ks = tile_span(P, kt * kBN);
-        const bool out0 = disjoint(ks, w0.band) && disjoint(ks, w0.sink);
-        const bool out1 = disjoint(ks, w1.band) && disjoint(ks, w1.sink);
-        if (out0 && out1) return;
+        if (disjoint(ks, w0.band) && disjoint(ks, w0.sink)) return;
         const SegInfo sk = seg_info(P, ks, khint);
         khint = sk.last;
-        const int c0 = out0 ? kEmpty : classify(P, q0, sq0, ks, sk);
-        const int c1 = out1 ? kEmpty : classify(P, q1, sq1, ks, sk);
-        if (c0 == kEmpty && c1 == kEmpty) return;
+        const int c0 = classify(P, q0, sq0, ks, sk);
+        if (c0 == kEmpty) return;
         const int slot = n & 1, use = n >> 1;
         if (use >= 1 && !(ok = mbar_wait(bar(L::kKEmpty + slot), (use - 1) & 1,
                                          abort_flag, P.status)))
           return;
-        sched[slot] = make_int4(kt, c0, c1, 0);
+        sched[slot] = make_int4(kt, c0, 0, 0);
         mbar_expect_tx(bar(L::kKFull + slot), L::kTileBytes);
         tma_load_4d(sbase + L::kK + slot * L::kTileBytes, &tm_k, bar(L::kKFull + slot), 0, g,
                     kt * kBN, bt);
         ++nk;
-        const int vslot = n % kVSlots, vuse = n / kVSlots;
-        if (vuse >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + vslot), (vuse - 1) & 1,
-                                          abort_flag, P.status)))
+        if (use >= 1 && !(ok = mbar_wait(bar(L::kVEmpty + slot), (use - 1) & 1,
+                                         abort_flag, P.status)))
           return;
-        mbar_expect_tx(bar(L::kVFull + vslot), L::kTileBytes);
+        mbar_expect_tx(bar(L::kVFull + slot), L::kTileBytes);
         // V^T map (key, d, head, batch): 128 keys x 128 d rows
-        tma_load_4d(sbase + L::kV + vslot * L::kTileBytes, &tm_vt, bar(L::kVFull + vslot),
+        tma_load_4d(sbase + L::kV + slot * L::kTileBytes, &tm_vt, bar(L::kVFull + slot),
                     kt * kBN, 0, g, bt);
         ++n;
       };
       for (int s = 0; s < P.cp && ok; ++s) {
         const int kap = (rho - s + P.cp) % P.cp;
         TileRun sr[2], br[2];
-        const int nsr = sinks.lo <= sinks.hi ? shard_runs(P, kap, sinks, sr) : 0;
-        const int nbr = shard_runs(P, kap, band, br);
+        const int nsr = w0.sink.lo <= w0.sink.hi ? shard_runs(P, kap, w0.sink, sr) : 0;
+        const int nbr = shard_runs(P, kap, w0.band, br);
         for (int ri = 0; ri < nsr && ok; ++ri)
           for (int kt = sr[ri].begin; kt < sr[ri].end && ok; ++kt) visit(kt);
         for (int ri = 0; ri < nbr && ok; ++ri)
@@ -212,130 +212,108 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
           sched[slot] = make_int4(kEnd, 0, 0, 0);
           mbar_arrive(bar(L::kKFull + slot));
         }
-        for (int m = (n >= kVSlots ? n - kVSlots : 0); m < n; ++m) {
-          const int sl = m % kVSlots, us = m / kVSlots;
-          if (!mbar_wait(bar(L::kVEmpty + sl), us & 1, abort_flag, P.status)) break;
-        }
+        // the last V^T tiles have been consumed before the CTA may exit
+        for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
+          if (!mbar_wait(bar(L::kVEmpty + (m & 1)), (m >> 1) & 1, abort_flag, P.status)) break;
       }
       if (*abort_flag) {
+        // aborted: let the copies already issued land before the CTA exits
         mbar_wait_drain(bar(L::kQFull), 0);
         for (int m = (nk >= 2 ? nk - 2 : 0); m < nk; ++m)
           mbar_wait_drain(bar(L::kKFull + (m & 1)), (m >> 1) & 1);
-        for (int m = (n >= kVSlots ? n - kVSlots : 0); m < n; ++m)
-          mbar_wait_drain(bar(L::kVFull + m % kVSlots), (m / kVSlots) & 1);
+        for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m)
+          mbar_wait_drain(bar(L::kVFull + (m & 1)), (m >> 1) & 1);
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // Same issue order as the bf16 forward: QK0(n), PV1(n-1), release V of
-    // n-1, QK1(n), release K of n, PV0(n). QK_i(n+1) follows PV_i(n) in issue
-    // order, so when S_i(n+1) is signalled the P_i tile has been read.
+    // Per key tile c: S = Q K^T; once the softmax has loaded S(c) into
+    // registers, the next key tile's Q K^T (its K slot loaded); then, once P(c)
+    // is in shared memory, O (+)= P V(c), whose commit frees the P tile and
+    // the V^T slot. The tensor core thus runs the next Q K^T while the
+    // softmax computes this tile's P.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_e4m3_f32(kBM, kBN);
       constexpr uint32_t kIdPV = idesc_e4m3_f32(kBM, kD);
-      const uint32_t s_tm[2] = {tmem, tmem + 128};
-      const uint32_t o_tm[2] = {tmem + 256, tmem + 256 + kD};
-      int cnt[2] = {0, 0};
-      // operand descriptors, built once (every tile of a buffer is a whole
-      // tile further on) and stepped by constants
+      const uint32_t s_tm = tmem, o_tm = tmem + 128;
+      // operand descriptors, built once and stepped by constants
       const uint64_t dq0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sbase + L::kK, 16, 1024);
       const uint64_t dp0 = sdesc_sw128(sbase + L::kP, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sbase + L::kV, 16, 1024);
-      bool ok = mbar_wait(bar(L::kQFull), 0, abort_flag, P.status);
-      auto qk = [&](int i, int slot) {
-        const uint64_t qd = sdesc_add(dq0, i * L::kTileBytes);
+      auto qk = [&](int slot) {
         const uint64_t kd = sdesc_add(dk0, slot * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kD / 32; ++kk)
-          mma_ss_f8(s_tm[i], sdesc_add(qd, 32 * kk), sdesc_add(kd, 32 * kk), kIdQK,
+          mma_ss_f8(s_tm, sdesc_add(dq0, 32 * kk), sdesc_add(kd, 32 * kk), kIdQK,
                     kk > 0 ? 1u : 0u);
-        mma_commit(bar(L::kSFull + i));
-        ++cnt[i];
+        mma_commit(bar(L::kSFull));
+        mma_commit(bar(L::kKEmpty + slot));
       };
-      auto pv = [&](int i, int slot, int use, int first) -> bool {
-        if (!mbar_wait(bar(L::kPFull + i), (cnt[i] - 1) & 1, abort_flag, P.status))
-          return false;
-        if (!mbar_wait(bar(L::kVFull + slot), use & 1, abort_flag, P.status))
-          return false;
+      bool ok = mbar_wait(bar(L::kQFull), 0, abort_flag, P.status);
+      bool more = false;
+      if (ok && (ok = mbar_wait(bar(L::kKFull + 0), 0, abort_flag, P.status))) {
+        const int4 e = sched[0];
+        more = e.x != kEnd;
+        if (more) {
+          tc_fence_after();
+          *info = make_int2(e.x, e.y);
+          mbar_arrive(bar(L::kInfoFull));
+          qk(0);
+        }
+      }
+      int c = 0;  // key tiles whose P V has been issued
+      while (ok && more) {
+        const int ns = (c + 1) & 1, nuse = (c + 1) >> 1;
+        if (!(ok = mbar_wait(bar(L::kKFull + ns), nuse & 1, abort_flag, P.status))) break;
+        const int4 e = sched[ns];
+        more = e.x != kEnd;
+        if (more) {
+          // S(c) is in the softmax's registers (and the softmax has read
+          // the entry of tile c): the next tile's S may take its columns
+          if (!(ok = mbar_wait(bar(L::kSFree), c & 1, abort_flag, P.status))) break;
+          tc_fence_after();
+          *info = make_int2(e.x, e.y);
+          mbar_arrive(bar(L::kInfoFull));
+          qk(ns);
+        }
+        const int slot = c & 1, use = c >> 1;
+        if (!(ok = mbar_wait(bar(L::kPFull), c & 1, abort_flag, P.status))) break;
+        if (!(ok = mbar_wait(bar(L::kVFull + slot), use & 1, abort_flag, P.status))) break;
         tc_fence_after();
-        const uint64_t pd = sdesc_add(dp0, i * L::kTileBytes);
         const uint64_t vd = sdesc_add(dv0, slot * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kBN / 32; ++kk)
-          mma_ss_f8(o_tm[i], sdesc_add(pd, 32 * kk), sdesc_add(vd, 32 * kk), kIdPV,
-                    (first && kk == 0) ? 0u : 1u);
-        return true;
-      };
-      int n = 0;
-      int first[2] = {1, 1};
-      int pend_slot = -1, pend_use = 0, pend_first = 0;
-      int prev_slot = -1;
-      while (ok) {
-        const int slot = n & 1, use = n >> 1;
-        const int vslot = n % kVSlots, vuse = n / kVSlots;
-        if (!(ok = mbar_wait(bar(L::kKFull + slot), use & 1, abort_flag, P.status))) break;
-        const int4 e = sched[slot];
-        if (e.x == kEnd) break;
-        tc_fence_after();
-        const bool e0 = e.y != kEmpty, e1 = e.z != kEmpty;
-        if (e0) {
-          info[0] = make_int2(e.x, e.y);
-          mbar_arrive(bar(L::kInfoFull + 0));
-          qk(0, slot);
-        }
-        if (pend_slot >= 0) {
-          if (!(ok = pv(1, pend_slot, pend_use, pend_first))) break;
-          pend_slot = -1;
-        }
-        if (prev_slot >= 0) mma_commit(bar(L::kVEmpty + prev_slot));
-        if (e1) {
-          info[1] = make_int2(e.x, e.z);
-          mbar_arrive(bar(L::kInfoFull + 1));
-          qk(1, slot);
-        }
-        mma_commit(bar(L::kKEmpty + slot));
-        if (e0) {
-          if (!(ok = pv(0, vslot, vuse, first[0]))) break;
-          first[0] = 0;
-        }
-        if (e1) {
-          pend_slot = vslot;
-          pend_use = vuse;
-          pend_first = first[1];
-          first[1] = 0;
-        }
-        prev_slot = vslot;
-        ++n;
+          mma_ss_f8(o_tm, sdesc_add(dp0, 32 * kk), sdesc_add(vd, 32 * kk), kIdPV,
+                    (c > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::kPFree));
+        mma_commit(bar(L::kVEmpty + slot));
+        ++c;
       }
-      if (ok && pend_slot >= 0) ok = pv(1, pend_slot, pend_use, pend_first);
-      if (ok && prev_slot >= 0) mma_commit(bar(L::kVEmpty + prev_slot));
-      for (int i = 0; i < 2; ++i) {
-        mma_commit(bar(L::kOFull + i));
-        info[i] = make_int2(kEnd, 0);
-        mbar_arrive(bar(L::kInfoFull + i));
-      }
+      mma_commit(bar(L::kOFull));
+      // every entry has been read (the last tile's P was waited for)
+      *info = make_int2(kEnd, 0);
+      mbar_arrive(bar(L::kInfoFull));
+      // nothing of ours may still run on the tensor core when TMEM is freed
       mma_commit(bar(L::kMmaDone));
       mbar_wait_drain(bar(L::kMmaDone), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int i = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;       // row within the tile = TMEM lane
-    const int prow = qbase0 + i * kBM + r;   // permuted query row
+    const int prow = qbase + r;              // permuted query row
     const RowMask rm = row_mask(P, nat_pos(P, prow));
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + 128 * i;
-    const uint32_t o_tm = tmem + lane_off + 256 + kD * i;
-    uint8_t* p_row = sm + L::kP + i * L::kTileBytes + r * 128;
+    const uint32_t s_tm = tmem + lane_off, o_tm = tmem + lane_off + 128;
+    uint8_t* p_row = sm + L::kP + r * 128;
     float m_run = -INFINITY, l_run = 0.f;  // l_run sums 2^4 p
     int c = 0;
     bool ok = true;
     while (true) {
-      ok = mbar_wait(bar(L::kInfoFull + i), c & 1, abort_flag, P.status);
+      ok = mbar_wait(bar(L::kInfoFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      const int2 inf = info[i];
+      const int2 inf = *info;
       if (inf.x == kEnd) break;
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
       if (inf.y == kMasked) {
@@ -345,13 +323,17 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) vis[ch] = col_bits(c0, 32 * ch) | col_bits(c1, 32 * ch);
       }
-      ok = mbar_wait(bar(L::kSFull + i), c & 1, abort_flag, P.status);
+      ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tm + 32 * ch, sr[ch]);
       tmem_wait_ld();
+      // S is in registers: the next key tile's Q K^T may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kSFree));
       if (inf.y == kMasked) {
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
@@ -376,6 +358,13 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       }
       l_run *= alpha;
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+      // the previous tile's P V has read the P tile and added into O (so the
+      // P tile and O may be written)
+      if (c > 0) {
+        ok = mbar_wait(bar(L::kPFree), (c - 1) & 1, abort_flag, P.status);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        tc_fence_after();
+      }
       // 2^4 p = exp2(s * scale_log2 - m + 4) <= 2^8, on packed fp32 pairs;
       // codes go to this row of the P tile, 16 keys per 16-byte chunk, in
       // the 128-byte swizzle (chunk k of row r at k ^ (r & 7))
@@ -412,8 +401,8 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
         f2_unpack(ls2[3], d0, d1);
         l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
       }
-      // O_i holds the PV of the previous tiles (complete: the commit that
-      // signalled S_i tracks every earlier MMA); rescale it to the new max
+      // rescale O (the previous tiles' P V, complete) to the new max before
+      // this tile's P V adds onto it
       if (__any_sync(0xffffffffu, need && c > 0)) {
 #pragma unroll
         for (int ch = 0; ch < kD / 32; ++ch) {
@@ -430,21 +419,22 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       fence_proxy_async_smem();  // the P tile is read next by the tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kPFull + i));
+      if (lane == 0) mbar_arrive(bar(L::kPFull));
       ++c;
     }
     // epilogue: v_descale * O / l -> bf16 rows, LSE = (m + log2 l - 4) ln 2.
     // The 64-column halves of the bf16 tile are staged in the 128-byte
-    // swizzle in this query tile's Q and P tiles (free: every MMA is done
-    // when O is) and one thread of the group stores them with TMA.
-    if (ok) ok = mbar_wait(bar(L::kOFull + i), 0, abort_flag, P.status);
+    // swizzle in the Q and P tiles (free: every MMA is done when O is) and
+    // one thread stores them with TMA.
+    if (ok) ok = mbar_wait(bar(L::kOFull), 0, abort_flag, P.status);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    const int unit = fwd_order(P, npairs).unit;
+    // the CTA's head and batch, recomputed (not kept live through the loop)
+    const int unit = batched_order(blockIdx.x, P.Hq * P.Bt, P.S / kBM, P.unit_batch).unit;
     const int h = fwd_head(P, unit), bt = fwd_batch(P, unit);
     if (ok) {
       const float mul = (l_run > 0.f) ? o_mul / l_run : 0.f;
-      uint8_t* stage[2] = {sm + L::kQ + i * L::kTileBytes, sm + L::kP + i * L::kTileBytes};
+      uint8_t* stage[2] = {sm + L::kQ, sm + L::kP};
 #pragma unroll
       for (int ch = 0; ch < kD / 32; ++ch) {
         uint32_t o[32];
@@ -466,11 +456,11 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kOStaged + i));
+      if (lane == 0) mbar_arrive(bar(L::kOStaged));
       if (quarter == 0 && lane == 0) {
-        if (mbar_wait(bar(L::kOStaged + i), 0, abort_flag, P.status)) {
+        if (mbar_wait(bar(L::kOStaged), 0, abort_flag, P.status)) {
           for (int hf = 0; hf < 2; ++hf)
-            tma_store_4d(&tm_o, smem_u32(stage[hf]), hf * 64, h, qbase0 + i * kBM, bt);
+            tma_store_4d(&tm_o, smem_u32(stage[hf]), hf * 64, h, qbase, bt);
           bulk_commit_group();
           // the tile has been read out of shared memory before the CTA exits
           // (the global writes complete on their own)
@@ -485,7 +475,7 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 256);
 }
 
 // [Bt][S][H][128] codes (tokens tok bytes apart) -> [Bt][H][128][S]: one
@@ -657,11 +647,11 @@ usp_status_t launch_fwd_fp8(const AttnParams& P, float v_descale, cudaStream_t s
   }
   AttnParams Pk = P;
   Pk.status = status;
-  // L2 batches as in the bf16 forward: about eight waves of CTAs, in whole
-  // GQA groups
+  // L2 batches as in the bf16 forward: about eight waves of CTAs (two per
+  // SM), in whole GQA groups
   {
-    const int npairs = P.S / (2 * kBM);
-    int per = (8 * sm_count() + npairs - 1) / npairs;
+    const int ntiles = P.S / kBM;
+    int per = (16 * sm_count() + ntiles - 1) / ntiles;
     per = (per + P.G - 1) / P.G * P.G;
     Pk.unit_batch = per < P.Hq * P.Bt ? per : P.Hq * P.Bt;
   }
@@ -673,7 +663,7 @@ usp_status_t launch_fwd_fp8(const AttnParams& P, float v_descale, cudaStream_t s
     if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(smem)", e);
     attr_set = true;
   }
-  const long long blocks = (long long)(P.S / (2 * kBM)) * P.Hq * P.Bt;
+  const long long blocks = (long long)(P.S / kBM) * P.Hq * P.Bt;
   {
     ProfScope ps(st, "attn_fwd_fp8");
     attn_fwd_fp8_kernel<<<(unsigned)blocks, kThreads, smem, st>>>(Pk, v_descale, mq, mk, mvt,
