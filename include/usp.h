@@ -363,7 +363,7 @@ usp_status_t usp_attn_bwd_qkvpacked(const void *qkv, const void *out,
  *      aligned, never NULL for S > 0 (it holds V transposed to
  *      [B][Hkv][128][S]); contents on entry irrelevant.
  * Errors: as usp_attn_fwd; USP_ERR_UNSUPPORTED for a head dim other than
- *      128 or a shard / zigzag chunk that is not a multiple of 256 tokens.
+ *      128 or a shard / zigzag chunk that is not a multiple of 128 tokens.
  */
 usp_status_t usp_attn_fwd_fp8(const void *q, const void *k, const void *v,
                               float q_descale, float k_descale, float v_descale,

@@ -578,8 +578,8 @@ int read_clear_fwd_fp8_status() {
 
 bool fwd_fp8_supported(const AttnParams& P) {
   if (P.D != kD) return false;
-  if (P.shard % (2 * kBM) != 0) return false;
-  if (P.layout == kZigzag && P.chunk % (2 * kBM) != 0) return false;
+  if (P.shard % kBM != 0) return false;
+  if (P.layout == kZigzag && P.chunk % kBM != 0) return false;
   return true;
 }
 

@@ -576,8 +576,8 @@ int read_clear_fwd_tc_status() {
 
 bool fwd_tc_supported(const AttnParams& P) {
   if (P.D != 128 && P.D != 64) return false;
-  if (P.shard % (2 * kBM) != 0) return false;
-  if (P.layout == kZigzag && P.chunk % (2 * kBM) != 0) return false;
+  if (P.shard % kBM != 0) return false;
+  if (P.layout == kZigzag && P.chunk % kBM != 0) return false;
   return true;
 }
 

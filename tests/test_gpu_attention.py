@@ -67,6 +67,10 @@ def test_layouts_and_degrees(layout, cp, ud):
     dict(layout="stripe", cp=4, S=1024, Hq=4, Hkv=2, window=300),
     dict(layout="zigzag", cp=2, S=1024, Hq=8, Hkv=2, window=250, sink_tokens=2),
     dict(layout="zigzag", cp=2, S=1024, Hq=4, Hkv=2, ud=2, window=333),
+    # 128-token zigzag chunks and stripe shards (one query tile per chunk)
+    dict(layout="zigzag", cp=4, S=1024, Hq=4, Hkv=2),
+    dict(layout="stripe", cp=4, S=512, Hq=4, Hkv=2),
+    dict(layout="contiguous", cp=8, S=1024, Hq=4, Hkv=2, ud=1, window=100),
 ])
 def test_bf16_d128(case, flags):
     w = BASE.replace(B=2, D=128, dtype="bf16", **case)

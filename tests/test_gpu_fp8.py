@@ -76,6 +76,9 @@ CASES = [
     dict(layout="contiguous", cp=2, S=1024, Hq=4, Hkv=2, window=300, sink_tokens=3),
     dict(layout="zigzag", cp=2, S=1024, Hq=4, Hkv=1, causal=False),
     dict(layout="zigzag", cp=2, S=2048, Hq=4, Hkv=2, ud=2),
+    # 128-token zigzag chunks and stripe shards: one query tile per chunk
+    dict(layout="zigzag", cp=4, S=1024, Hq=4, Hkv=2),
+    dict(layout="stripe", cp=4, S=512, Hq=4, Hkv=2),
 ]
 
 
@@ -131,7 +134,7 @@ def test_fp8_rejections():
     with pytest.raises(usp.UspError, match="INVALID_ARG"):
         usp.attn_forward_fp8(z, z, z, 0.0, 1.0, 1.0, cp=1)          # descale 0
     with pytest.raises(usp.UspError, match="UNSUPPORTED"):
-        usp.attn_forward_fp8(z, z, z, 1.0, 1.0, 1.0, cp=4)          # 128-token shards
+        usp.attn_forward_fp8(z, z, z, 1.0, 1.0, 1.0, cp=8)          # 64-token shards
 
 
 def test_fp8_full_size_sampled_rows():

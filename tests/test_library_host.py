@@ -209,7 +209,7 @@ def test_python_saved_exchange_needs_the_workspace():
 
 
 def fp8_fwd(lib, **over):
-    # zigzag, ring of 2, S = 1024: 256-token chunks, the smallest the kernel takes
+    # zigzag, ring of 2, S = 1024: 256-token chunks (the kernel takes multiples of 128)
     a = dict(q=FAKE, k=FAKE, v=FAKE, qd=1.0, kd=1.0, vd=1.0, out=FAKE, lse=FAKE, B=1, S=1024,
              Hq=4, Hkv=2, D=128, scale=0.0, causal=1, window=0, sink=0, cu=None, cp=2, ud=1,
              layout=1, flags=0, ws=None, wsb=0, stream=None)
@@ -226,7 +226,7 @@ def fp8_fwd(lib, **over):
     (dict(qd=0.0), 1), (dict(vd=-1.0), 1), (dict(kd=float("inf")), 1),
     (dict(q=FAKE + 8), 3),
     (dict(v=None), 1),
-    (dict(cp=4), 2),                # 128-token chunks are below the 256-token pair
+    (dict(cp=8), 2),                # 64-token chunks are below the 128-token tile
     (dict(Hq=3), 1),
 ])
 def test_fp8_forward_rejects_before_launch(lib, over, code):
