@@ -547,6 +547,9 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   const int ntiles = P.S / kBM;
   int per = (16 * sm_count() + ntiles - 1) / ntiles;
   per = (per + P.G - 1) / P.G * P.G;
+  // packed sequences: one batch (a query tile only meets the keys of its own
+  // sequence; measured 4 % faster on the 128K packed batch than 8 waves)
+  if (P.cu != nullptr) per = P.Hq * P.Bt;
   Pk.unit_batch = per < P.Hq * P.Bt ? per : P.Hq * P.Bt;
   const int smem = Smem<D>::kAlloc;
   static bool attr_set = false;
