@@ -1,17 +1,18 @@
 """Benchmark of the sequence-parallel attention hot path on GB300.
 
 One step is one training pass of the whole path over one batch of synthetic
-input in natural sequence order, through the library's C ABI:
-  usp_attn_fwd  (extract q, k, v into rank-major order fused with the
-                 Ulysses seq->head exchange, ring attention with the fused
-                 LSE merge, head->seq exchange fused with the restore of O)
-  -> usp_attn_bwd  (the same for dO in and dQ, dK, dV out, reusing the
-                    forward's copies of q, k, v, O; Delta, dQ/dK/dV with the
-                    ring return).
-Without Ulysses (ud = 1) the extract and restore run as layout permutes.
+input in natural sequence order, through the library's C ABI: usp_attn_fwd
+then usp_attn_bwd with the natural-order flag. For windows, packed batches
+and sequences up to 16K tokens (contiguous or zigzag) the tensor-core kernels
+read and write the caller's tensors in place; otherwise the layout's extract
+(fused with the Ulysses seq->head exchange when ud > 1) and restore run inside
+the calls, and the backward reuses the forward's rank-major copies. Both
+passes run the ring attention with the fused LSE merge; the backward adds
+Delta and the ring return of dK/dV.
 The metric is useful attention TFLOP/s (masked pairs not counted; backward
-= 2.5x forward). The standalone tree/linear LSE merge is timed on its own
-workload in the same run and reported under "merge".
+= 2.5x forward). The standalone tree/linear LSE merge, the layout permute and
+the Ulysses exchange are timed on their own in the same run ("merge",
+"permute").
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torchrun; every rank runs its own replica of the
@@ -531,6 +532,34 @@ def main():
     except Exception as e:  # report, do not hide
         merge_res = {"error": repr(e)}
 
+    # standalone layout permute and Ulysses exchange on the step's q tensor
+    # (the natural-order step above runs neither: its kernels read the
+    # caller's tensors in place); both are HBM-bound copies, 2 bytes moved
+    # per byte of the tensor, and the tensor exceeds L2
+    permute_res = None
+    try:
+        src = x["q"]
+        dst = torch.empty_like(src)
+        Bp = 1 if w.varlen else w.B
+        Hp, Sp = w.Hq, w.S
+        by = 2 * src.numel() * src.element_size()
+        kinds = [("extract", 1)] + ([("seq2head", w.ud)] if w.ud > 1 else [])
+        for kind, udp in kinds:
+            fn = lambda: usp.usp_permute(src, dst, kind, w.layout, Bp, Sp, Hp, w.D, w.cp, udp,  # noqa: E731
+                                         src.element_size())
+            for _ in range(3):
+                fn()
+            pms = timed(fn, 10)
+            gbs = by / (pms * 1e-3) / 1e9
+            permute_res = permute_res or {}
+            permute_res[kind] = {"layout": w.layout, "cp": w.cp, "ud": udp,
+                                 "tensor_bytes": src.numel() * src.element_size(),
+                                 "ms": pms, "bytes": by, "GB_s": gbs,
+                                 "frac_hbm": gbs / pk["hbm_gbs"]}
+        del dst
+    except Exception as e:  # report, do not hide
+        permute_res = {"error": repr(e)}
+
     # decode step (split-KV partials over the sharded cache + tree merge) on
     # its own workload: HBM-bound, reported against the copy bandwidth
     decode_res = None
@@ -744,7 +773,7 @@ def main():
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches * args.steps), "clocks": clocks,
         "gate": gate, "kernels": kernels, "kernels_rank_major": rank_major,
-        "merge": merge_res, "decode": decode_res,
+        "merge": merge_res, "permute": permute_res, "decode": decode_res,
         "fp8": fp8_res,
     }
     if rank == 0:
