@@ -56,6 +56,13 @@ constexpr float kRescaleThreshold = 4.0f;  // log2 units; bounds p by 2^4
 constexpr float kPLog2 = 4.0f;             // P codes hold 2^4 p
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Largest of three values in one instruction (three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 struct Smem8 {
   static constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 one-byte codes
   static constexpr int kQ = 0;
@@ -341,14 +348,17 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
           for (int j = 0; j < 32; ++j)
             if (!((vis[ch] >> j) & 1u)) sr[ch][j] = __float_as_uint(-INFINITY);
       }
+      // row max as 8 independent chains of three-input maxima (a single
+      // chain is latency-bound)
       float m8[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[t >> 5][t & 31]);
 #pragma unroll
-      for (int j = 8; j < 128; ++j)
-        m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int j = 8; j < 128; j += 2)
+        m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(sr[j >> 5][j & 31]),
+                                 __uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]));
+      float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                       fmaxf(m8[6], m8[7]));
       mx *= P.scale_log2;
       const bool need = mx > m_run + kRescaleThreshold;
       float alpha = 1.f;
@@ -358,22 +368,15 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       }
       l_run *= alpha;
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      // the previous tile's P V has read the P tile and added into O (so the
-      // P tile and O may be written)
-      if (c > 0) {
-        ok = mbar_wait(bar(L::kPFree), (c - 1) & 1, abort_flag, P.status);
-        if (!(ok = __all_sync(0xffffffffu, ok))) break;
-        tc_fence_after();
-      }
-      // 2^4 p = exp2(s * scale_log2 - m + 4) <= 2^8, on packed fp32 pairs;
-      // codes go to this row of the P tile, 16 keys per 16-byte chunk, in
-      // the 128-byte swizzle (chunk k of row r at k ^ (r & 7))
+      // 2^4 p = exp2(s * scale_log2 - m + 4) <= 2^8, on packed fp32 pairs,
+      // as e4m3 codes held in registers (w[4 ck + q]: keys 16 ck + 4 q ..
+      // 16 ck + 4 q + 3) until the previous tile's P V has read the P tile
       const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
       const uint64_t nm2 = f2_pack(kPLog2 - msub, kPLog2 - msub);
       uint64_t ls2[4] = {0, 0, 0, 0};
+      uint32_t w[32];
 #pragma unroll
       for (int ck = 0; ck < 8; ++ck) {
-        uint32_t w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float pp[4];
@@ -389,9 +392,8 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
             pp[2 * t + 1] = ex2(x1);
             ls2[(2 * q + t) & 3] = f2_add(ls2[(2 * q + t) & 3], f2_pack(pp[2 * t], pp[2 * t + 1]));
           }
-          w[q] = pack_e4m3(pp[0], pp[1]) | (pack_e4m3(pp[2], pp[3]) << 16);
+          w[4 * ck + q] = pack_e4m3(pp[0], pp[1]) | (pack_e4m3(pp[2], pp[3]) << 16);
         }
-        *reinterpret_cast<uint4*>(p_row + ((ck ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       {
         float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -401,6 +403,19 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
         f2_unpack(ls2[3], d0, d1);
         l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
       }
+      // the previous tile's P V has read the P tile and added into O (so the
+      // P tile and O may be written)
+      if (c > 0) {
+        ok = mbar_wait(bar(L::kPFree), (c - 1) & 1, abort_flag, P.status);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        tc_fence_after();
+      }
+      // this row of the P tile, 16 keys per 16-byte chunk, in the 128-byte
+      // swizzle (chunk k of row r at k ^ (r & 7))
+#pragma unroll
+      for (int ck = 0; ck < 8; ++ck)
+        *reinterpret_cast<uint4*>(p_row + ((ck ^ (r & 7)) << 4)) =
+            make_uint4(w[4 * ck], w[4 * ck + 1], w[4 * ck + 2], w[4 * ck + 3]);
       // rescale O (the previous tiles' P V, complete) to the new max before
       // this tile's P V adds onto it
       if (__any_sync(0xffffffffu, need && c > 0)) {
