@@ -139,3 +139,44 @@ def test_simt_and_tensor_core_paths_agree():
     b = run_forward(usp, w, x, dev, usp.FLAG_FORCE_SIMT)
     assert np.abs(to_np(a[0]) - to_np(b[0])).max() <= 2e-2
     assert np.abs(to_np(a[1]) - to_np(b[1])).max() <= 1e-3
+
+
+# Edge cases of the visibility rule on the tensor-core kernels (bf16, D=128,
+# ring chunks of 128 tokens or more).
+EDGE = {
+    "window1_sinks5": dict(layout="contiguous", cp=4, S=1024, Hq=4, Hkv=2, window=1,
+                           sink_tokens=5),
+    "sinks_past_window": dict(layout="stripe", cp=4, S=1024, Hq=4, Hkv=2, window=64,
+                              sink_tokens=200),
+    "window_wider_than_sequence": dict(layout="zigzag", cp=4, S=1024, Hq=4, Hkv=2,
+                                       window=5000),
+    "window_equal_to_sequence": dict(layout="zigzag", cp=2, S=1024, Hq=4, Hkv=2, window=1024),
+    "multi_query_ring8": dict(layout="zigzag", cp=8, S=2048, Hq=8, Hkv=1),
+    "one_head_per_ulysses_rank": dict(layout="zigzag", cp=2, S=1024, Hq=4, Hkv=4, ud=4),
+    "non_causal_window": dict(layout="contiguous", cp=4, S=1024, Hq=4, Hkv=2, window=200,
+                              causal=False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_bf16_visibility_edge_cases(name):
+    check(BASE.replace(B=2, D=128, dtype="bf16", **EDGE[name]))
+
+
+def test_window_of_one_returns_own_value():
+    """A window of one key (the query's own): the softmax over a single score
+    is 1, so O_i = v_i and dV = dO bit for bit, LSE_i = scale * q_i . k_i,
+    and dQ, dK vanish up to the rounding of dP - Delta (two fp32 sums of the
+    same 128 products, in different orders)."""
+    dev = device()
+    w = BASE.replace(B=2, S=1024, Hq=4, Hkv=4, D=128, dtype="bf16", cp=4, layout="zigzag",
+                     window=1)
+    x = make_inputs(w, seed=11, with_grad=True)
+    fwd = run_forward(usp, w, x, dev)
+    assert torch.equal(fwd[0].cpu(), x["v"])
+    q, k = to_np(x["q"]), to_np(x["k"])
+    lse = lse_to_natural(to_np(fwd[1]), w)
+    assert np.abs(lse - w.scale * np.einsum("bshd,bshd->bhs", q, k)).max() <= 1e-3
+    dq, dk, dv = run_backward(usp, w, x, dev, fwd)
+    assert torch.equal(dv.cpu(), x["dout"])
+    assert float(dq.abs().max()) <= 2e-3 and float(dk.abs().max()) <= 2e-3
