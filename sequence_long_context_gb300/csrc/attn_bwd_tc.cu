@@ -351,11 +351,14 @@ attn_bwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kSFull));
-        // the previous dQ must have left [128,256) (and the reduction warp
-        // must have read its entry) before dP^T and the next entry
+        // the dO tile (its load does not depend on this tile's progress)
+        // is checked first, so that its check is not added to the wait for
+        // the previous dQ, which must have left [128,256) (and the
+        // reduction warp must have read its entry) before dP^T and the
+        // next entry
+        if (!(ok = mbar_wait(bar(L::kDOFull + slot), use & 1, abort_flag, P.status))) break;
         if (n > 0 && !(ok = mbar_wait(bar(L::kDQEmpty), (n - 1) & 1, abort_flag, P.status)))
           break;
-        if (!(ok = mbar_wait(bar(L::kDOFull + slot), use & 1, abort_flag, P.status))) break;
         tc_fence_after();
         info[1] = e;
         mbar_arrive(bar(L::kInfoQ));

@@ -63,6 +63,35 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// Non-blocking test of one mbarrier phase (acquire semantics, like a wait).
+__device__ __forceinline__ uint32_t mbar_test1(uint32_t a, uint32_t pa) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(a), "r"(pa)
+      : "memory");
+  return r;
+}
+// Non-blocking tests of two mbarrier phases issued back to back: bit 0 set
+// if the phase of a with parity pa has completed, bit 1 likewise for b.
+__device__ __forceinline__ uint32_t mbar_test2(uint32_t a, uint32_t pa, uint32_t b,
+                                               uint32_t pb) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@q or.b32 %0, %0, 2;\n\t}"
+      : "=r"(r)
+      : "r"(a), "r"(pa), "r"(b), "r"(pb)
+      : "memory");
+  return r;
+}
+
 struct Smem8 {
   static constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 one-byte codes
   static constexpr int kQ = 0;
@@ -284,9 +313,11 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
           mbar_arrive(bar(L::kInfoFull));
           qk(ns);
         }
+        // the V^T slot (usually loaded long before) first, so that its check
+        // is not added to the wait for P
         const int slot = c & 1, use = c >> 1;
-        if (!(ok = mbar_wait(bar(L::kPFull), c & 1, abort_flag, P.status))) break;
         if (!(ok = mbar_wait(bar(L::kVFull + slot), use & 1, abort_flag, P.status))) break;
+        if (!(ok = mbar_wait(bar(L::kPFull), c & 1, abort_flag, P.status))) break;
         tc_fence_after();
         const uint64_t vd = sdesc_add(dv0, slot * L::kTileBytes);
 #pragma unroll
@@ -317,8 +348,9 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
     float m_run = -INFINITY, l_run = 0.f;  // l_run sums 2^4 p
     int c = 0;
     bool ok = true;
+    uint32_t ahead = 0;  // bit 0 / 1: tile c's entry / S found there ahead
     while (true) {
-      ok = mbar_wait(bar(L::kInfoFull), c & 1, abort_flag, P.status);
+      ok = (ahead & 1u) || mbar_wait(bar(L::kInfoFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       const int2 inf = *info;
       if (inf.x == kEnd) break;
@@ -330,7 +362,7 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) vis[ch] = col_bits(c0, 32 * ch) | col_bits(c1, 32 * ch);
       }
-      ok = mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
+      ok = (ahead & 2u) || mbar_wait(bar(L::kSFull), c & 1, abort_flag, P.status);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -371,6 +403,10 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       // 2^4 p = exp2(s * scale_log2 - m + 4) <= 2^8, on packed fp32 pairs,
       // as e4m3 codes held in registers (w[4 ck + q]: keys 16 ck + 4 q ..
       // 16 ck + 4 q + 3) until the previous tile's P V has read the P tile
+      // the previous tile's P V is usually done by the end of this tile's
+      // exponentials: its phase is tested now, the test's latency
+      // overlapping them, and waited for afterwards only if it was not
+      const uint32_t p_free = (c == 0) ? 1u : mbar_test1(bar(L::kPFree), (c - 1) & 1);
       const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
       const uint64_t nm2 = f2_pack(kPLog2 - msub, kPLog2 - msub);
       uint64_t ls2[4] = {0, 0, 0, 0};
@@ -405,11 +441,15 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       }
       // the previous tile's P V has read the P tile and added into O (so the
       // P tile and O may be written)
-      if (c > 0) {
+      // the next tile's entry and S (its Q K^T was issued when this S was
+      // loaded) are tested now, the tests' latency overlapping the P stores;
+      // the next iteration waits only for what was not there
+      ahead = mbar_test2(bar(L::kInfoFull), (c + 1) & 1, bar(L::kSFull), (c + 1) & 1);
+      if (!__all_sync(0xffffffffu, p_free != 0u)) {
         ok = mbar_wait(bar(L::kPFree), (c - 1) & 1, abort_flag, P.status);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
-        tc_fence_after();
       }
+      tc_fence_after();
       // this row of the P tile, 16 keys per 16-byte chunk, in the 128-byte
       // swizzle (chunk k of row r at k ^ (r & 7))
 #pragma unroll
