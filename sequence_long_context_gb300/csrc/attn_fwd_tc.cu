@@ -50,6 +50,16 @@ constexpr int kEnd = -1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Named CTA barrier 1, the set-up barrier: the producer warp only arrives
+// (the barriers it initialised are ready), the other warps wait for all
+// threads (and for the tensor-memory base the MMA warp allocated).
+__device__ __forceinline__ void setup_arrive(int threads) {
+  asm volatile("bar.arrive 1, %0;" ::"r"(threads) : "memory");
+}
+__device__ __forceinline__ void setup_sync(int threads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
+
 // CTA order: units are query heads ordered (kv head, batch, query head of
 // the group), so a batch of consecutive units shares K/V.
 __device__ __forceinline__ int fwd_head(const AttnParams& P, int unit) {
@@ -66,13 +76,14 @@ __device__ __forceinline__ int fwd_batch(const AttnParams& P, int unit) {
 // rescaled then; exact, since O / l and m + log l do not depend on which m
 // was used), the row sum accumulated on packed pairs; P is handed over in
 // two halves (b_ph, then b_p). Epilogue: O / l as bf16 rows staged in
-// `stage` (128-byte swizzle) and stored with TMA by the first thread, LSE =
+// `stage` (128-byte swizzle), each warp's 32 rows stored with TMA by its
+// first thread, LSE =
 // (m + log2 l) ln 2. b_* are the tile's barriers; nranks is the CTA order's
 // ranks per unit (to recompute the head late).
 template <int D, int kHalfBytes, int kHalves>
 __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* info,
                                              uint32_t b_info, uint32_t b_s, uint32_t b_ph,
-                                             uint32_t b_p, uint32_t b_o, uint32_t b_staged,
+                                             uint32_t b_p, uint32_t b_o,
                                              uint32_t s_tm,
                                              uint32_t o_tm, uint8_t* stage,
                                              const CUtensorMap* tm_o, int qrow0, int quarter,
@@ -191,8 +202,8 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
   }
   // epilogue: O / l -> bf16 rows, LSE = (m + log2 l) ln 2. The rows are
   // staged in the 128-byte swizzle in this query tile's shared-memory slot
-  // (free: every Q K^T has completed when O is) and one thread of the
-  // group stores the tile with TMA.
+  // (free: every Q K^T has completed when O is) and each warp stores its
+  // own 32 rows with TMA.
   if (ok) ok = mbar_wait(b_o, 0, abort_flag, P.status);
   ok = __all_sync(0xffffffffu, ok);
   tc_fence_after();
@@ -228,18 +239,17 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& P, const int2* in
     }
     fence_proxy_async_smem();  // the staged rows are read next by the TMA unit
     __syncwarp();
-    if (lane == 0) mbar_arrive(b_staged);
-    if (quarter == 0 && lane == 0) {
-      if (mbar_wait(b_staged, 0, abort_flag, P.status)) {
-        const TensorPos t = tensor_pos(P, h, qrow0, bt, P.Hq);
-        for (int hf = 0; hf < kHalves; ++hf)
-          tma_store_4d(tm_o, smem_u32(stage + hf * kHalfBytes), hf * 64, t.h, t.row,
-                       t.b);
-        bulk_commit_group();
-        // the tile has been read out of shared memory before the CTA exits
-        // (the global writes complete on their own)
-        bulk_wait_group_read0();
-      }
+    if (lane == 0) {
+      // this warp's 32 rows (1024-byte aligned in the staging, so the
+      // swizzle phase is the tile's), no wait for the other warps
+      const TensorPos t = tensor_pos(P, h, qrow0, bt, P.Hq);
+      for (int hf = 0; hf < kHalves; ++hf)
+        tma_store_4d(tm_o, smem_u32(stage + hf * kHalfBytes + quarter * 32 * 128), hf * 64,
+                     t.h, t.row + 32 * quarter, t.b);
+      bulk_commit_group();
+      // the rows have been read out of shared memory before the CTA exits
+      // (the global writes complete on their own)
+      bulk_wait_group_read0();
     }
     P.lse[lse_index(P, bt, h, prow)] =
         (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
@@ -267,7 +277,7 @@ struct Smem {
   static constexpr int kBar = kV + kTileBytes;
   static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 2, kVFull = 3, kVEmpty = 4,
                        kSFull = 5, kPFull = 6, kOFull = 7, kInfoFull = 8, kMmaDone = 9,
-                       kOStaged = 10, kPHalf = 11, kNumBars = 12;
+                       kPHalf = 10, kNumBars = 11;
   static constexpr int kSched = (kBar + 8 * kNumBars + 15) / 16 * 16;  // int4
   static constexpr int kInfo = kSched + 16;                           // int2
   static constexpr int kMisc = kInfo + 16;                            // tmem base, abort
@@ -326,7 +336,6 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(L::kOFull), 1);
     mbar_init(bar(L::kInfoFull), 1);
     mbar_init(bar(L::kMmaDone), 1);
-    mbar_init(bar(L::kOStaged), kBM / 32);  // one arrival per softmax warp
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tm_q);
@@ -342,10 +351,19 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     tmem_alloc(sbase + L::kMisc, 256);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
+  // The producer needs nothing from the other warps' set-up: it signals that
+  // the barriers exist and goes straight on to classify and load the key
+  // tiles, so that the first K/V loads overlap the tensor-memory allocation.
+  uint32_t tmem = 0;  // the producer never uses it
+  if (warp == kProducerWarp) {
+    __syncwarp();
+    setup_arrive(kThreads);
+  } else {
+    tc_fence_before();
+    setup_sync(kThreads);
+    tc_fence_after();
+    tmem = *tmem_holder;
+  }
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -471,7 +489,7 @@ attn_fwd_tc_kernel(const AttnParams P, const __grid_constant__ CUtensorMap tm_q,
     softmax_tile<D, L::kHalfBytes, L::kHalves>(
         P, info, bar(L::kInfoFull), bar(L::kSFull), bar(L::kPHalf), bar(L::kPFull),
         bar(L::kOFull),
-        bar(L::kOStaged), tmem + lane_off, tmem + lane_off + 128, sm + L::kQ, &tm_o, qbase,
+        tmem + lane_off, tmem + lane_off + 128, sm + L::kQ, &tm_o, qbase,
         quarter, lane, ntiles, abort_flag);
   }
 
@@ -494,10 +512,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [Bt][S][H][D] bf16 -> 4-D map (D, H, S, Bt), box (64, 1, 128, 1), 128B swizzle.
+// [Bt][S][H][D] bf16 -> 4-D map (D, H, S, Bt), box (64, 1, rows, 1), 128B swizzle.
 // tok: elements between tokens (0: dense H*D; 3*H*D in a packed q/k/v tensor)
 bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
-              long long tok = 0) {
+              long long tok = 0, int rows = kBM) {
   if (tok == 0) tok = (long long)H * D;
   auto fn = encode_fn();
   if (!fn) {
@@ -507,7 +525,7 @@ bool make_map(CUtensorMap* m, const void* base, int Bt, int S, int H, int D,
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)Bt};
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)tok * 2,
                            (cuuint64_t)S * tok * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kBM, 1};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -530,7 +548,7 @@ usp_status_t launch_d(const AttnParams& P, cudaStream_t st) {
   if (!make_map(&mq, P.q, Bm, P.S, P.Hq * hm, D, P.qkv_tok) ||
       !make_map(&mk, P.k, Bm, P.S, P.Hkv * hm, D, P.qkv_tok) ||
       !make_map(&mv, P.v, Bm, P.S, P.Hkv * hm, D, P.qkv_tok) ||
-      !make_map(&mo, P.o, Bm, P.S, P.Hq * hm, D))
+      !make_map(&mo, P.o, Bm, P.S, P.Hq * hm, D, 0, 32))  // O: one warp's rows
     return USP_ERR_CUDA;  // detail recorded by make_map
   static int* status = nullptr;
   if (status == nullptr) {
