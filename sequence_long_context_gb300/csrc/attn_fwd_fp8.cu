@@ -400,13 +400,13 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
       }
       l_run *= alpha;
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      // 2^4 p = exp2(s * scale_log2 - m + 4) <= 2^8, on packed fp32 pairs,
-      // as e4m3 codes held in registers (w[4 ck + q]: keys 16 ck + 4 q ..
-      // 16 ck + 4 q + 3) until the previous tile's P V has read the P tile
       // the previous tile's P V is usually done by the end of this tile's
       // exponentials: its phase is tested now, the test's latency
       // overlapping them, and waited for afterwards only if it was not
       const uint32_t p_free = (c == 0) ? 1u : mbar_test1(bar(L::kPFree), (c - 1) & 1);
+      // 2^4 p = exp2(s * scale_log2 - m + 4) <= 2^8, on packed fp32 pairs,
+      // as e4m3 codes held in registers (w[4 ck + q]: keys 16 ck + 4 q ..
+      // 16 ck + 4 q + 3) until the previous tile's P V has read the P tile
       const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
       const uint64_t nm2 = f2_pack(kPLog2 - msub, kPLog2 - msub);
       uint64_t ls2[4] = {0, 0, 0, 0};
