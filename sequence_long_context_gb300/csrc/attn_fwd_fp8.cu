@@ -63,6 +63,19 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// Four fp32 -> four e4m3 codes in one 32-bit word (a in the low byte):
+// round to nearest even, finite values beyond the largest code saturate.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
 // Non-blocking test of one mbarrier phase (acquire semantics, like a wait).
 __device__ __forceinline__ uint32_t mbar_test1(uint32_t a, uint32_t pa) {
   uint32_t r;
@@ -428,7 +441,7 @@ attn_fwd_fp8_kernel(const AttnParams P, float o_mul,
             pp[2 * t + 1] = ex2(x1);
             ls2[(2 * q + t) & 3] = f2_add(ls2[(2 * q + t) & 3], f2_pack(pp[2 * t], pp[2 * t + 1]));
           }
-          w[4 * ck + q] = pack_e4m3(pp[0], pp[1]) | (pack_e4m3(pp[2], pp[3]) << 16);
+          w[4 * ck + q] = pack_e4m3x4(pp[0], pp[1], pp[2], pp[3]);
         }
       }
       {
